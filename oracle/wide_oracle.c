@@ -1,0 +1,197 @@
+/*
+ * wide_oracle.c -- plain, slow, obviously-correct CPU restatement of the
+ * group-masked projections of WIDE (token-level dynamic width pruning).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Only the test-suite, the smoke check and the
+ * benchmark's CPU-baseline leg may load this library.  The product path (the
+ * CUDA library) shares no code, header, table or helper with this file.
+ *
+ * Source: "WIDE: Boosting Adaptive LLM Inference via Token-level Dynamic
+ * Width Pruning" (arXiv 2607.28418, HTML version).
+ *   - Sec. 3.3, Eq. 7: per-routing-column SortDesc giving the reordered mask
+ *     and the gather/scatter index I.
+ *   - App. B, "metadata shared by all three kernels": the index identity
+ *     reordered[j,g] = M[I[j,g], g]; (B,T) flattened to M rows.
+ *   - Sec. 3.1, Eq. 3: FFN unit, ((phi(X Wg^T) (.) (X Wu^T)) (.)_G M) Wd^T.
+ *   - Sec. 3.1, Eq. 2: attention unit (q_proj pruned on out-features,
+ *     o_proj on in-features), G = (Hq/Hk) d.
+ *   - App. B, "Implementation of GEMM-K", Eq. 21:
+ *     C[m,n] = sum_g M[m,g] sum_{k in K_g} A[m,k] B[n,k].
+ *
+ * Arithmetic: every bf16 input is decoded exactly to double and every sum
+ * is accumulated in double (the pages fix no precision; double makes the
+ * rounding of this file negligible against the GPU's bf16/fp32 path).
+ * Loops run in the order of the definitions; the only parallelism is an
+ * OpenMP loop over independent tokens (rows).
+ *
+ * Readings where the pages are silent (each is listed in the design notes):
+ *   - phi is SiLU, x * sigmoid(x) (Llama backbones, Sec. 4.1).
+ *   - SortDesc is stable: active rows first, then inactive rows, each part
+ *     in ascending original row index; I is a full permutation.
+ *   - A mask byte != 0 means "active".
+ *   - Channel f belongs to group floor(f / G) (contiguous groups, Sec. 3.1).
+ *   - Weights are stored [out_features, in_features] (B in R^{N x K}, Sec. 3.3).
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <string.h>
+
+/* Exact bf16 -> double: a bf16 value is the upper half of an IEEE float. */
+static double bf16_to_double(uint16_t bits)
+{
+    uint32_t u = ((uint32_t)bits) << 16;
+    float f;
+    memcpy(&f, &u, sizeof f);
+    return (double)f;
+}
+
+/* SiLU, the reading of the element-wise activation phi of Eq. 3. */
+static double silu(double a)
+{
+    return a / (1.0 + exp(-a));
+}
+
+int oracle_version(void) { return 1; }
+
+/*
+ * Eq. 7 (Sec. 3.3) and App. B Algorithm 1: for every routing column g,
+ * SortDesc(M[:,g]) -- a stable partition of the rows, active first.
+ *   mask   : uint8 [T, n_groups] row-major, != 0 means active
+ *   perm   : int32 [n_groups, T]  (perm[g*T + j] = I[j, g])
+ *   counts : int32 [n_groups]     (length of the active prefix)
+ */
+void oracle_reorder(const uint8_t *mask, int T, int n_groups,
+                    int32_t *perm, int32_t *counts)
+{
+    for (int g = 0; g < n_groups; ++g) {
+        int c = 0;
+        for (int t = 0; t < T; ++t)
+            if (mask[(size_t)t * n_groups + g] != 0)
+                perm[(size_t)g * T + c++] = t;
+        counts[g] = c;
+        for (int t = 0; t < T; ++t)
+            if (mask[(size_t)t * n_groups + g] == 0)
+                perm[(size_t)g * T + c++] = t;
+    }
+}
+
+/*
+ * GEMM-MN without activation (Sec. 3.1 Eq. 2 for q_proj; App. B
+ * "Implementation of GEMM-MN"): Y[t, n] = M[t, n/G] * sum_k X[t,k] W[n,k].
+ *   X : bf16 [T, K], W : bf16 [N, K], mask : uint8 [T, N/G], Y : double [R, N]
+ *   rows : optional list of R token indices to evaluate (NULL = all T rows,
+ *          R = T); output row i is token rows[i].
+ */
+void oracle_proj_mn(const uint16_t *X, const uint16_t *W, const uint8_t *mask,
+                    int T, int K, int N, int G,
+                    const int32_t *rows, int n_rows, double *Y)
+{
+    const int n_groups = N / G;
+    const int R = rows ? n_rows : T;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < R; ++i) {
+        const int t = rows ? rows[i] : i;
+        for (int n = 0; n < N; ++n) {
+            double y = 0.0;
+            if (mask[(size_t)t * n_groups + n / G] != 0) {
+                for (int k = 0; k < K; ++k)
+                    y += bf16_to_double(X[(size_t)t * K + k]) *
+                         bf16_to_double(W[(size_t)n * K + k]);
+            }
+            Y[(size_t)i * N + n] = y;
+        }
+    }
+}
+
+/*
+ * FFN up/gate half of Eq. 3 (Sec. 3.1), GEMM-MN with the fused activation:
+ *   H[t, f] = M[t, f/G] * silu(sum_d X[t,d] Wg[f,d]) * (sum_d X[t,d] Wu[f,d])
+ *   X : bf16 [T, D], Wg, Wu : bf16 [F, D], mask : uint8 [T, F/G],
+ *   H : double [R, F] (rows as in oracle_proj_mn).
+ */
+void oracle_gate_up(const uint16_t *X, const uint16_t *Wg, const uint16_t *Wu,
+                    const uint8_t *mask, int T, int D, int F, int G,
+                    const int32_t *rows, int n_rows, double *H)
+{
+    const int n_groups = F / G;
+    const int R = rows ? n_rows : T;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < R; ++i) {
+        const int t = rows ? rows[i] : i;
+        for (int f = 0; f < F; ++f) {
+            double h = 0.0;
+            if (mask[(size_t)t * n_groups + f / G] != 0) {
+                double a = 0.0, b = 0.0;
+                for (int d = 0; d < D; ++d) {
+                    const double x = bf16_to_double(X[(size_t)t * D + d]);
+                    a += x * bf16_to_double(Wg[(size_t)f * D + d]);
+                    b += x * bf16_to_double(Wu[(size_t)f * D + d]);
+                }
+                h = silu(a) * b;
+            }
+            H[(size_t)i * F + f] = h;
+        }
+    }
+}
+
+/*
+ * GEMM-K, App. B Eq. 21 (down_proj / o_proj, pruned on in-features):
+ *   Y[t, n] = sum_g M[t,g] sum_{k in K_g} A[t,k] W[n,k],  K_g = [gG, (g+1)G)
+ *   A : bf16 [T, K], W : bf16 [N, K], mask : uint8 [T, K/G],
+ *   Y : double [R, N].  Entries of A in inactive groups never contribute.
+ */
+void oracle_proj_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask,
+                   int T, int K, int N, int G,
+                   const int32_t *rows, int n_rows, double *Y)
+{
+    const int n_groups = K / G;
+    const int R = rows ? n_rows : T;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < R; ++i) {
+        const int t = rows ? rows[i] : i;
+        for (int n = 0; n < N; ++n) {
+            double y = 0.0;
+            for (int g = 0; g < n_groups; ++g) {
+                if (mask[(size_t)t * n_groups + g] == 0)
+                    continue;
+                for (int k = g * G; k < (g + 1) * G; ++k)
+                    y += bf16_to_double(A[(size_t)t * K + k]) *
+                         bf16_to_double(W[(size_t)n * K + k]);
+            }
+            Y[(size_t)i * N + n] = y;
+        }
+    }
+}
+
+/*
+ * Whole masked FFN of Eq. 3: Y = ((silu(X Wg^T) (.) X Wu^T) (.)_G M) Wd^T,
+ * with the intermediate kept in double (never rounded).
+ *   X : bf16 [T, D], Wg, Wu : bf16 [F, D], Wd : bf16 [D, F],
+ *   mask : uint8 [T, F/G], Y : double [R, D].
+ */
+void oracle_ffn(const uint16_t *X, const uint16_t *Wg, const uint16_t *Wu,
+                const uint16_t *Wd, const uint8_t *mask,
+                int T, int D, int F, int G,
+                const int32_t *rows, int n_rows, double *Y,
+                double *scratch /* [R, F] */)
+{
+    const int R = rows ? n_rows : T;
+    const int n_groups = F / G;
+    oracle_gate_up(X, Wg, Wu, mask, T, D, F, G, rows, n_rows, scratch);
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int i = 0; i < R; ++i) {
+        const int t = rows ? rows[i] : i;
+        for (int n = 0; n < D; ++n) {
+            double y = 0.0;
+            for (int g = 0; g < n_groups; ++g) {
+                if (mask[(size_t)t * n_groups + g] == 0)
+                    continue;
+                for (int f = g * G; f < (g + 1) * G; ++f)
+                    y += scratch[(size_t)i * F + f] *
+                         bf16_to_double(Wd[(size_t)n * F + f]);
+            }
+            Y[(size_t)i * D + n] = y;
+        }
+    }
+}
