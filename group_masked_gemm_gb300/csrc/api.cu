@@ -1,0 +1,264 @@
+// api.cu -- the extern "C" boundary of libwide.so (declared in include/wide.h):
+// host-side argument validation, TMA descriptor encoding, kernel dispatch
+// (prefill tcgen05 kernels vs. small-T decode kernels) and the device status
+// word.  No call allocates, frees or synchronises (except wide_device_status).
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
+#include "../../include/wide.h"
+#include "common.cuh"
+#include "internal.h"
+
+namespace wide {
+size_t decode_mn_smem_bytes(int T, int K, int n_groups);
+int gemm_k_max_groups();
+}  // namespace wide
+
+namespace {
+
+constexpr int kVersion = 1 * 10000 + 0 * 100 + 0;
+constexpr int kDecodeMaxT = 16;
+constexpr int kMaxDevices = 64;
+
+// First device-side failure since the last wide_device_status() call.
+__device__ int g_device_status = 0;
+
+std::mutex g_mutex;
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+int g_num_sms[kMaxDevices] = {0};
+int *g_status_ptr[kMaxDevices] = {nullptr};
+
+wide_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? WIDE_OK : WIDE_ERR_CUDA; }
+
+bool aligned16(const void *p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+bool good_ptr(const void *p) { return p != nullptr && aligned16(p); }
+
+bool good_group(int G) { return G == 64 || G == 128 || G == 256 || G == 512; }
+
+// Group sizes come from the tile-size set {2^k : k >= 4} (Sec. 3.1); members
+// of the set outside {64..512} are valid but not implemented.
+wide_status_t bad_group_status(int G) {
+    return (G >= 16 && (G & (G - 1)) == 0) ? WIDE_ERR_UNSUPPORTED : WIDE_ERR_INVALID_ARG;
+}
+
+struct DeviceCtx {
+    int num_sms;
+    int *status;
+};
+
+wide_status_t device_ctx(DeviceCtx *ctx) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return WIDE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_mutex);
+    if (g_num_sms[dev] == 0) {
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+            return WIDE_ERR_CUDA;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_device_status) != cudaSuccess) return WIDE_ERR_CUDA;
+        g_status_ptr[dev] = static_cast<int *>(p);
+        g_num_sms[dev] = n;
+    }
+    if (g_encode == nullptr) {
+        void *fn = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000,
+                                             cudaEnableDefault, &q) != cudaSuccess ||
+            q != cudaDriverEntryPointSuccess || fn == nullptr)
+            return WIDE_ERR_CUDA;
+        g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+    }
+    ctx->num_sms = g_num_sms[dev];
+    ctx->status = g_status_ptr[dev];
+    return WIDE_OK;
+}
+
+// 2-D bf16 tensor [rows, cols] (cols contiguous), box {64 cols, box_rows},
+// 128-byte swizzle; out-of-range elements read as zero.
+wide_status_t encode_bf16_2d(CUtensorMap *m, const void *base, long long rows, long long cols,
+                             int box_rows) {
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(cols), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(cols) * 2};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1u, 1u};
+    CUresult r = g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void *>(base), dims,
+                          strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                          CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                          CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? WIDE_OK : WIDE_ERR_CUDA;
+}
+
+// Shared validation of GEMM-MN style calls; out features N grouped by G.
+wide_status_t check_mn(const void *X, const void *W0, const void *W1, const void *mask,
+                       const void *perm, const void *counts, int T, int K, int N, int G,
+                       const void *out, bool need_w1) {
+    if (!good_ptr(X) || !good_ptr(W0) || (need_w1 && !good_ptr(W1)) || !good_ptr(mask) ||
+        !good_ptr(out))
+        return WIDE_ERR_INVALID_ARG;
+    if (T < 1 || K < 64 || N < 64 || K % 64 || N % 64) return WIDE_ERR_INVALID_ARG;
+    if (!good_group(G)) return bad_group_status(G);
+    if (N % G) return WIDE_ERR_INVALID_ARG;
+    if (N / G > wide::kMaxGroups) return WIDE_ERR_UNSUPPORTED;
+    if (T > kDecodeMaxT && (!good_ptr(perm) || !good_ptr(counts))) return WIDE_ERR_INVALID_ARG;
+    if ((perm != nullptr && !aligned16(perm)) || (counts != nullptr && !aligned16(counts)))
+        return WIDE_ERR_INVALID_ARG;
+    return WIDE_OK;
+}
+
+wide_status_t check_k(const void *A, const void *W, const void *mask, int T, int K, int N, int G,
+                      const void *out, const void *ws, size_t ws_bytes) {
+    if (!good_ptr(A) || !good_ptr(W) || !good_ptr(mask) || !good_ptr(out))
+        return WIDE_ERR_INVALID_ARG;
+    if (T < 1 || K < 64 || N < 64 || K % 64 || N % 64) return WIDE_ERR_INVALID_ARG;
+    if (!good_group(G)) return bad_group_status(G);
+    if (K % G) return WIDE_ERR_INVALID_ARG;
+    if (K / G > wide::gemm_k_max_groups()) return WIDE_ERR_UNSUPPORTED;
+    const size_t need = wide_gemm_k_workspace_size(T, K, N, G);
+    if (need > 0 && (ws == nullptr || ws_bytes < need)) return WIDE_ERR_WORKSPACE;
+    return WIDE_OK;
+}
+
+wide_status_t run_mn(wide::MNMode mode, const uint16_t *X, const uint16_t *W0,
+                     const uint16_t *W1, const uint8_t *mask, const int32_t *perm,
+                     const int32_t *counts, int T, int K, int N, int G, uint16_t *out,
+                     void *stream) {
+    DeviceCtx ctx;
+    wide_status_t st = device_ctx(&ctx);
+    if (st != WIDE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    const bool gate_up = mode == wide::MNMode::kGateUp;
+    if (T <= kDecodeMaxT && wide::decode_mn_smem_bytes(T, K, N / G) <= 200 * 1024) {
+        wide::DecodeArgs a{X, W0, gate_up ? W1 : nullptr, mask, out, T, K, N, G};
+        return from_cuda(wide::launch_decode_mn(mode, a, ctx.num_sms, s));
+    }
+    if (perm == nullptr || counts == nullptr) return WIDE_ERR_INVALID_ARG;
+    const int bn = gate_up ? (G == 64 ? 64 : 128) : (G == 64 ? 64 : G == 128 ? 128 : 256);
+    CUtensorMap tmA, tmB0, tmB1;
+    if ((st = encode_bf16_2d(&tmA, X, T, K, 1)) != WIDE_OK) return st;
+    if ((st = encode_bf16_2d(&tmB0, W0, N, K, bn)) != WIDE_OK) return st;
+    if ((st = encode_bf16_2d(&tmB1, gate_up ? W1 : W0, N, K, bn)) != WIDE_OK) return st;
+    wide::MNArgs a{perm, counts, out, T, K, N, G, ctx.status};
+    return from_cuda(wide::launch_gemm_mn(mode, bn, tmA, tmB0, tmB1, a, ctx.num_sms, s));
+}
+
+wide_status_t run_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask, int T, int K,
+                    int N, int G, uint16_t *out, void *stream) {
+    DeviceCtx ctx;
+    wide_status_t st = device_ctx(&ctx);
+    if (st != WIDE_OK) return st;
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T <= kDecodeMaxT) {
+        wide::DecodeArgs a{A, W, nullptr, mask, out, T, K, N, G};
+        return from_cuda(wide::launch_decode_k(a, ctx.num_sms, s));
+    }
+    const int bn = N % 256 == 0 ? 256 : N % 128 == 0 ? 128 : 64;
+    CUtensorMap tmA, tmB;
+    if ((st = encode_bf16_2d(&tmA, A, T, K, 128)) != WIDE_OK) return st;
+    if ((st = encode_bf16_2d(&tmB, W, N, K, bn)) != WIDE_OK) return st;
+    wide::KArgs a{mask, out, T, K, N, G, ctx.status};
+    return from_cuda(wide::launch_gemm_k(bn, tmA, tmB, a, ctx.num_sms, s));
+}
+
+}  // namespace
+
+extern "C" {
+
+const char *wide_status_string(int status) {
+    switch (status) {
+        case WIDE_OK: return "WIDE_OK";
+        case WIDE_ERR_INVALID_ARG: return "WIDE_ERR_INVALID_ARG";
+        case WIDE_ERR_UNSUPPORTED: return "WIDE_ERR_UNSUPPORTED";
+        case WIDE_ERR_WORKSPACE: return "WIDE_ERR_WORKSPACE";
+        case WIDE_ERR_CUDA: return "WIDE_ERR_CUDA";
+        case WIDE_ERR_TIMEOUT: return "WIDE_ERR_TIMEOUT";
+        default: return "WIDE_ERR_UNKNOWN";
+    }
+}
+
+int wide_version(void) { return kVersion; }
+
+int wide_num_sms(void) {
+    DeviceCtx ctx;
+    return device_ctx(&ctx) == WIDE_OK ? ctx.num_sms : 0;
+}
+
+size_t wide_reorder_workspace_size(int T, int n_groups) {
+    (void)T;
+    (void)n_groups;
+    return 0;
+}
+
+wide_status_t wide_reorder_masks(const uint8_t *mask, int T, int n_groups, int32_t *perm,
+                                 int32_t *counts, void *ws, size_t ws_bytes, void *stream) {
+    (void)ws;
+    (void)ws_bytes;
+    if (!good_ptr(mask) || !good_ptr(perm) || !good_ptr(counts)) return WIDE_ERR_INVALID_ARG;
+    if (T < 1 || n_groups < 1 || n_groups > 65535) return WIDE_ERR_INVALID_ARG;
+    if (static_cast<long long>(T) * n_groups > (1ll << 40)) return WIDE_ERR_INVALID_ARG;
+    return from_cuda(wide::launch_reorder(mask, T, n_groups, perm, counts,
+                                          static_cast<cudaStream_t>(stream)));
+}
+
+wide_status_t wide_gemm_mn_gate_up(const uint16_t *X, const uint16_t *W_gate,
+                                   const uint16_t *W_up, const uint8_t *mask,
+                                   const int32_t *perm, const int32_t *counts, int T, int d_model,
+                                   int d_ffn, int G, uint16_t *H, void *stream) {
+    wide_status_t st = check_mn(X, W_gate, W_up, mask, perm, counts, T, d_model, d_ffn, G, H, true);
+    if (st != WIDE_OK) return st;
+    return run_mn(wide::MNMode::kGateUp, X, W_gate, W_up, mask, perm, counts, T, d_model, d_ffn,
+                  G, H, stream);
+}
+
+wide_status_t wide_proj_mn(const uint16_t *X, const uint16_t *W, const uint8_t *mask,
+                           const int32_t *perm, const int32_t *counts, int T, int K, int N, int G,
+                           uint16_t *Y, void *stream) {
+    wide_status_t st = check_mn(X, W, nullptr, mask, perm, counts, T, K, N, G, Y, false);
+    if (st != WIDE_OK) return st;
+    return run_mn(wide::MNMode::kPlain, X, W, nullptr, mask, perm, counts, T, K, N, G, Y, stream);
+}
+
+size_t wide_gemm_k_workspace_size(int T, int K, int N, int G) {
+    (void)T;
+    (void)K;
+    (void)N;
+    (void)G;
+    return 0;
+}
+
+wide_status_t wide_gemm_k_down(const uint16_t *H, const uint16_t *W_down, const uint8_t *mask,
+                               const int32_t *perm, const int32_t *counts, int T, int d_ffn,
+                               int d_model, int G, uint16_t *Y, void *ws, size_t ws_bytes,
+                               void *stream) {
+    (void)perm;
+    (void)counts;
+    wide_status_t st = check_k(H, W_down, mask, T, d_ffn, d_model, G, Y, ws, ws_bytes);
+    if (st != WIDE_OK) return st;
+    return run_k(H, W_down, mask, T, d_ffn, d_model, G, Y, stream);
+}
+
+wide_status_t wide_proj_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask,
+                          const int32_t *perm, const int32_t *counts, int T, int K, int N, int G,
+                          uint16_t *Y, void *ws, size_t ws_bytes, void *stream) {
+    (void)perm;
+    (void)counts;
+    wide_status_t st = check_k(A, W, mask, T, K, N, G, Y, ws, ws_bytes);
+    if (st != WIDE_OK) return st;
+    return run_k(A, W, mask, T, K, N, G, Y, stream);
+}
+
+wide_status_t wide_device_status(void *stream) {
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return WIDE_ERR_CUDA;
+    int v = 0;
+    if (cudaMemcpyFromSymbol(&v, g_device_status, sizeof v) != cudaSuccess) return WIDE_ERR_CUDA;
+    if (v != 0) {
+        const int zero = 0;
+        if (cudaMemcpyToSymbol(g_device_status, &zero, sizeof zero) != cudaSuccess)
+            return WIDE_ERR_CUDA;
+    }
+    return static_cast<wide_status_t>(v);
+}
+
+}  // extern "C"

@@ -1,0 +1,342 @@
+// gemm_k.cu -- GEMM-K on tcgen05 (WIDE, App. B "Implementation of GEMM-K",
+// Eq. 21; Sec. 3.1 Eq. 2-3 for o_proj / down_proj).
+//
+//   Y[t, n] = sum_g M[t,g] sum_{k in [gG,(g+1)G)} A[t,k] W[n,k]
+//
+// GB300 design: a persistent CTA owns an output tile of 128 tokens (natural
+// order) x BN columns and keeps its fp32 accumulator in TMEM for the whole
+// reduction, adding the groups in ascending order -- a per-token ordered
+// reduction with no atomics, no workspace and a deterministic result.  The
+// routing mask is applied inside the tensor core: every tcgen05.mma of group
+// g carries a disable-output-lane mask whose bit is set for the tokens of the
+// tile with M[t,g] = 0, so their accumulator rows are left untouched (the
+// l=2 predicate of Eq. 20, per TMEM lane).  A group with no active token in
+// the tile is skipped entirely (copies, MMAs and barriers; the l=0
+// predicate), and values of A inside inactive groups never reach Y.
+//
+// Warps: 0 TMA producer, 1 TMEM owner + MMA issuer, 2 mask builder (turns the
+// tile's mask block into lane masks and a list of live groups, double
+// buffered), 3..6 epilogue (TMEM -> bf16 rows of Y, then re-zeroes the
+// accumulator for its next tile).
+#include "common.cuh"
+#include "internal.h"
+
+namespace wide {
+namespace {
+
+constexpr int BM = 128;
+constexpr int BK = 64;
+constexpr int kThreads = 224;
+constexpr int kMaxKGroups = 512;
+constexpr int kSmemBudget = 225 * 1024;
+
+template <int BN>
+struct KCfg {
+    static constexpr int A_BYTES = BM * BK * 2;
+    static constexpr int B_BYTES = BN * BK * 2;
+    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
+    // per mask buffer: lane masks [ng][4] + live-group list [ng] + count
+    static constexpr int MASK_BUF_BYTES = kMaxKGroups * 16 + kMaxKGroups * 4 + 16;
+    static constexpr int BAR_BYTES = 256;
+    static constexpr int STAGES_FIT =
+        (kSmemBudget - 1024 - 2 * MASK_BUF_BYTES - BAR_BYTES) / STAGE_BYTES;
+    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
+    static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
+    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * MASK_BUF_BYTES + BAR_BYTES;
+    static_assert(STAGES >= 2, "pipeline needs two stages");
+    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
+};
+
+struct MaskBuf {
+    uint32_t *lanes;  // [ng][4] disable-output-lane words
+    int *live;        // [ng] live groups, ascending
+    int *n_live;
+};
+
+template <int BN>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_k_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
+                  const KArgs args) {
+    using C = KCfg<BN>;
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint8_t *stages = smem;
+    uint8_t *mask_area = smem + C::STAGES * C::STAGE_BYTES;
+    MaskBuf mb[2];
+    for (int b = 0; b < 2; ++b) {
+        uint8_t *base = mask_area + b * C::MASK_BUF_BYTES;
+        mb[b].lanes = reinterpret_cast<uint32_t *>(base);
+        mb[b].live = reinterpret_cast<int *>(base + kMaxKGroups * 16);
+        mb[b].n_live = reinterpret_cast<int *>(base + kMaxKGroups * 20);
+    }
+    uint64_t *bars = reinterpret_cast<uint64_t *>(mask_area + 2 * C::MASK_BUF_BYTES);
+    uint64_t *full = bars;
+    uint64_t *empty = bars + C::STAGES;
+    uint64_t *tfull = bars + 2 * C::STAGES;
+    uint64_t *tempty = tfull + 2;
+    uint64_t *mfull = tempty + 2;   // mask builder -> producer + MMA
+    uint64_t *mempty = mfull + 2;   // producer + MMA -> mask builder
+    uint64_t *final_bar = mempty + 2;
+    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(final_bar + 1);
+    volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int T = args.T;
+    const int ng = args.K / args.G;
+    const int m_tiles = (T + BM - 1) / BM;
+    const int n_tiles = args.N / BN;
+    const int n_items = m_tiles * n_tiles;
+    const int kb_per_group = args.G / BK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < C::STAGES; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int b = 0; b < 2; ++b) {
+            mbar_init(&tfull[b], 1);
+            mbar_init(&tempty[b], 4);
+            mbar_init(&mfull[b], 1);
+            mbar_init(&mempty[b], 2);
+        }
+        mbar_init(final_bar, 1);
+        *s_abort = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0 && lane == 0) {
+        prefetch_tmap(&tmA);
+        prefetch_tmap(&tmB);
+    }
+    if (warp == 1) {
+        tmem_alloc(s_tmem, C::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem_base = *s_tmem;
+    // Accumulators start at zero: every MMA accumulates (lanes it skips must
+    // keep the value of the groups already added).
+    if (warp >= 3) {
+        const int quad = warp & 3;
+        uint32_t z[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) z[q] = 0u;
+        for (int col = 0; col < 2 * BN; col += 32)
+            tmem_st32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + col, z);
+        tmem_st_wait();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+
+    if (warp == 2) {
+        // ===================== mask builder =====================
+        int b = 0;
+        uint32_t bphase = 0;
+        for (int i = blockIdx.x; i < n_items && !*s_abort; i += gridDim.x) {
+            const int mt = i / n_tiles;
+            const int m0 = mt * BM;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&mempty[b], bphase ^ 1u, args.status);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) { *s_abort = 1; break; }
+            int n_live = 0;
+            constexpr int kU = 8;  // groups per batch of independent loads
+            for (int g0 = 0; g0 < ng; g0 += kU) {
+                uint8_t v[kU][4];
+#pragma unroll
+                for (int u = 0; u < kU; ++u)
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) {
+                        const int t = m0 + 32 * q + lane;
+                        const int g = g0 + u;
+                        v[u][q] = (t < T && g < ng) ? args.mask[static_cast<size_t>(t) * ng + g] : 0;
+                    }
+#pragma unroll
+                for (int u = 0; u < kU; ++u) {
+                    const int g = g0 + u;
+                    if (g >= ng) break;
+                    uint32_t w[4];
+#pragma unroll
+                    for (int q = 0; q < 4; ++q) w[q] = __ballot_sync(0xffffffffu, v[u][q] != 0);
+                    const bool live = (w[0] | w[1] | w[2] | w[3]) != 0u;
+                    if (lane < 4) mb[b].lanes[g * 4 + lane] = ~w[lane];
+                    if (live) {
+                        if (lane == 0) mb[b].live[n_live] = g;
+                        ++n_live;
+                    }
+                }
+            }
+            if (lane == 0) *mb[b].n_live = n_live;
+            __threadfence_block();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mfull[b]);  // release semantics publish the buffer
+            if (++b == 2) { b = 0; bphase ^= 1u; }
+        }
+    } else if (warp == 0) {
+        // ===================== TMA producer =====================
+        int stage = 0;
+        uint32_t phase = 0;
+        uint32_t used = 0, last_parity = 0;
+        int b = 0;
+        uint32_t bphase = 0;
+        for (int i = blockIdx.x; i < n_items && !*s_abort; i += gridDim.x) {
+            const int mt = i / n_tiles, nt = i - mt * n_tiles;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&mfull[b], bphase, args.status);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) { *s_abort = 1; break; }
+            const int n_live = *mb[b].n_live;
+            for (int li = 0; li < n_live && ok; ++li) {
+                const int g = mb[b].live[li];
+                for (int kb = 0; kb < kb_per_group; ++kb) {
+                    if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, args.status);
+                    ok = __shfl_sync(0xffffffffu, ok, 0);
+                    if (!ok) break;
+                    if (lane == 0) {
+                        uint8_t *sa = stages + stage * C::STAGE_BYTES;
+                        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                        const int kx = g * args.G + kb * BK;
+                        tma_load_2d(sa, &tmA, &full[stage], kx, mt * BM);
+                        tma_load_2d(sa + C::A_BYTES, &tmB, &full[stage], kx, nt * BN);
+                    }
+                    used |= 1u << stage;
+                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
+                    if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+                }
+            }
+            if (!ok) { *s_abort = 1; break; }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&mempty[b]);
+            if (++b == 2) { b = 0; bphase ^= 1u; }
+        }
+        if (lane == 0)
+            for (int s = 0; s < C::STAGES; ++s)
+                if (used & (1u << s)) mbar_wait(&full[s], (last_parity >> s) & 1u, args.status);
+        __syncwarp();
+    } else if (warp == 1) {
+        // ===================== tcgen05 issuer =====================
+        if (lane == 0) {
+            int stage = 0;
+            uint32_t phase = 0;
+            int acc = 0;
+            uint32_t acc_phase = 0;
+            int b = 0;
+            uint32_t bphase = 0;
+            for (int i = blockIdx.x; i < n_items && !*s_abort; i += gridDim.x) {
+                if (!mbar_wait(&mfull[b], bphase, args.status)) { *s_abort = 1; break; }
+                if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, args.status)) { *s_abort = 1; break; }
+                tc_fence_after();
+                const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
+                const int n_live = *mb[b].n_live;
+                bool ok = true;
+                for (int li = 0; li < n_live && ok; ++li) {
+                    const int g = mb[b].live[li];
+                    const uint32_t l0 = mb[b].lanes[g * 4 + 0], l1 = mb[b].lanes[g * 4 + 1];
+                    const uint32_t l2 = mb[b].lanes[g * 4 + 2], l3 = mb[b].lanes[g * 4 + 3];
+                    for (int kb = 0; kb < kb_per_group; ++kb) {
+                        if (!mbar_wait(&full[stage], phase, args.status)) { ok = false; break; }
+                        tc_fence_after();
+                        const uint32_t a0 = smem_u32(stages + stage * C::STAGE_BYTES);
+                        const uint32_t b0 = a0 + C::A_BYTES;
+#pragma unroll
+                        for (int kk = 0; kk < BK / 16; ++kk)
+                            mma_bf16_lanemask(d, sw128_kmajor_desc(a0 + kk * 32),
+                                              sw128_kmajor_desc(b0 + kk * 32), C::IDESC, l0, l1, l2,
+                                              l3, 1u);
+                        mma_commit(&empty[stage]);
+                        if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+                    }
+                }
+                if (!ok) { *s_abort = 1; break; }
+                mma_commit(&tfull[acc]);
+                mbar_arrive(&mempty[b]);
+                if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+                if (++b == 2) { b = 0; bphase ^= 1u; }
+            }
+            mma_commit(final_bar);
+            mbar_wait(final_bar, 0, args.status);
+        }
+        __syncwarp();
+    } else {
+        // ===================== epilogue (warps 3..6) =====================
+        const int quad = warp & 3;
+        const int row = quad * 32 + lane;
+        int acc = 0;
+        uint32_t acc_phase = 0;
+        uint32_t z[32];
+#pragma unroll
+        for (int q = 0; q < 32; ++q) z[q] = 0u;
+        for (int i = blockIdx.x; i < n_items && !*s_abort; i += gridDim.x) {
+            const int mt = i / n_tiles, nt = i - mt * n_tiles;
+            const int t = mt * BM + row;
+            int ok = 1;
+            if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, args.status);
+            ok = __shfl_sync(0xffffffffu, ok, 0);
+            if (!ok) { *s_abort = 1; break; }
+            tc_fence_after();
+            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
+                                   static_cast<uint32_t>(acc * BN);
+            uint16_t *dst = args.out + static_cast<size_t>(t) * args.N + nt * BN;
+#pragma unroll 1
+            for (int cb = 0; cb < BN; cb += 32) {
+                uint32_t yr[32];
+                tmem_ld32(taddr + cb, yr);
+                tmem_ld_wait();
+                tmem_st32(taddr + cb, z);
+                if (t < T) {
+#pragma unroll
+                    for (int q = 0; q < 4; ++q)
+                        st_global_v4(dst + cb + 8 * q,
+                                     pack_bf16x2(__uint_as_float(yr[8 * q + 0]), __uint_as_float(yr[8 * q + 1])),
+                                     pack_bf16x2(__uint_as_float(yr[8 * q + 2]), __uint_as_float(yr[8 * q + 3])),
+                                     pack_bf16x2(__uint_as_float(yr[8 * q + 4]), __uint_as_float(yr[8 * q + 5])),
+                                     pack_bf16x2(__uint_as_float(yr[8 * q + 6]), __uint_as_float(yr[8 * q + 7])));
+                }
+            }
+            tmem_st_wait();
+            tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&tempty[acc]);
+            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 1) {
+        tc_fence_after();
+        tmem_dealloc(tmem_base, C::TMEM_COLS);
+    }
+}
+
+template <int BN>
+cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a, int num_sms,
+                     cudaStream_t s) {
+    using C = KCfg<BN>;
+    auto kern = gemm_k_kernel<BN>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
+    if (e != cudaSuccess) return e;
+    const int m_tiles = (a.T + BM - 1) / BM;
+    const int items = m_tiles * (a.N / BN);
+    const int grid = items < num_sms ? items : num_sms;
+    kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(tmA, tmB, a);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+int gemm_k_max_groups() { return kMaxKGroups; }
+
+cudaError_t launch_gemm_k(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a,
+                          int num_sms, cudaStream_t s) {
+    if (bn == 256) return launch_t<256>(tmA, tmB, a, num_sms, s);
+    if (bn == 128) return launch_t<128>(tmA, tmB, a, num_sms, s);
+    if (bn == 64) return launch_t<64>(tmA, tmB, a, num_sms, s);
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace wide

@@ -1,0 +1,58 @@
+// internal.h -- host-side launchers shared between the C-ABI layer (api.cu)
+// and the kernel translation units.  Arguments are validated by api.cu.
+#pragma once
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace wide {
+
+// GEMM-MN flavours: plain projection or fused silu(gate) * up.
+enum class MNMode { kPlain = 0, kGateUp = 1 };
+
+struct MNArgs {
+    const int32_t *perm;    // [n_groups, T]
+    const int32_t *counts;  // [n_groups]
+    uint16_t *out;          // bf16 [T, n_out]
+    int T, K, n_out, G;
+    int *status;
+};
+
+struct KArgs {
+    const uint8_t *mask;  // [T, n_groups]
+    uint16_t *out;        // bf16 [T, N]
+    int T, K, N, G;
+    int *status;
+};
+
+struct DecodeArgs {
+    const uint16_t *x;     // bf16 [T, K]
+    const uint16_t *w0;    // bf16 [N, K]  (gate, or the only weight)
+    const uint16_t *w1;    // bf16 [N, K]  (up) or nullptr
+    const uint8_t *mask;   // [T, n_groups]
+    uint16_t *out;         // bf16 [T, N]
+    int T, K, N, G;
+};
+
+cudaError_t launch_reorder(const uint8_t *mask, int T, int n_groups, int32_t *perm,
+                           int32_t *counts, cudaStream_t s);
+
+// tmA: gather4 map over the token-row operand [T, K] (box 64 x 1, 128-B swizzle)
+// tmB0/tmB1: tiled maps over the weights [n_out, K] (box 64 x bn, 128-B swizzle)
+cudaError_t launch_gemm_mn(MNMode mode, int bn, const CUtensorMap &tmA, const CUtensorMap &tmB0,
+                           const CUtensorMap &tmB1, const MNArgs &a, int num_sms,
+                           cudaStream_t s);
+
+// tmA: tiled map over the token-row operand [T, K] (box 64 x 128)
+// tmB: tiled map over the weights [N, K] (box 64 x bn)
+cudaError_t launch_gemm_k(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
+                          const KArgs &a, int num_sms, cudaStream_t s);
+
+cudaError_t launch_decode_mn(MNMode mode, const DecodeArgs &a, int num_sms, cudaStream_t s);
+cudaError_t launch_decode_k(const DecodeArgs &a, int num_sms, cudaStream_t s);
+
+// Largest n_groups the GEMM kernels keep in shared memory.
+constexpr int kMaxGroups = 1024;
+
+}  // namespace wide

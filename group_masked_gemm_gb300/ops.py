@@ -1,0 +1,209 @@
+"""ctypes binding over libwide.so (the C ABI of include/wide.h).
+
+Argument marshalling only: every step of the path runs in the library's CUDA
+kernels.  Tensors are torch CUDA tensors (bf16 weights/activations, uint8
+masks, int32 perm/counts); the binding passes their device pointers and the
+current CUDA stream.  The library itself never allocates: the helpers below
+allocate outputs with torch only when no ``out=`` tensor is given.
+
+If libwide.so is missing or fails to load, every call raises -- there is no
+CPU fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import threading
+
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libwide.so")
+
+STATUS = {0: "WIDE_OK", 1: "WIDE_ERR_INVALID_ARG", 2: "WIDE_ERR_UNSUPPORTED",
+          3: "WIDE_ERR_WORKSPACE", 4: "WIDE_ERR_CUDA", 5: "WIDE_ERR_TIMEOUT"}
+
+_lock = threading.Lock()
+_lib = None
+
+
+class WideError(RuntimeError):
+    def __init__(self, fn: str, status: int):
+        super().__init__(f"{fn} failed: {STATUS.get(status, status)}")
+        self.status = status
+
+
+def lib():
+    """Load libwide.so (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        with _lock:
+            if _lib is None:
+                if not os.path.exists(LIB_PATH):
+                    raise RuntimeError(
+                        f"{LIB_PATH} is missing: build it with "
+                        "`python -m group_masked_gemm_gb300.build` (nvcc, sm_103a)")
+                L = ctypes.CDLL(LIB_PATH)
+                p, i, sz = ctypes.c_void_p, ctypes.c_int, ctypes.c_size_t
+                L.wide_status_string.argtypes = [i]
+                L.wide_status_string.restype = ctypes.c_char_p
+                L.wide_version.restype = i
+                L.wide_num_sms.restype = i
+                L.wide_reorder_workspace_size.argtypes = [i, i]
+                L.wide_reorder_workspace_size.restype = sz
+                L.wide_reorder_masks.argtypes = [p, i, i, p, p, p, sz, p]
+                L.wide_gemm_mn_gate_up.argtypes = [p, p, p, p, p, p, i, i, i, i, p, p]
+                L.wide_gemm_k_down.argtypes = [p, p, p, p, p, i, i, i, i, p, p, sz, p]
+                L.wide_proj_mn.argtypes = [p, p, p, p, p, i, i, i, i, p, p]
+                L.wide_proj_k.argtypes = [p, p, p, p, p, i, i, i, i, p, p, sz, p]
+                L.wide_gemm_k_workspace_size.argtypes = [i, i, i, i]
+                L.wide_gemm_k_workspace_size.restype = sz
+                L.wide_device_status.argtypes = [p]
+                for fn in ("wide_reorder_masks", "wide_gemm_mn_gate_up", "wide_gemm_k_down",
+                           "wide_proj_mn", "wide_proj_k", "wide_device_status"):
+                    getattr(L, fn).restype = i
+                _lib = L
+    return _lib
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _check(fn, status):
+    if status != 0:
+        raise WideError(fn, status)
+
+
+def _need(t, dtype, name, ndim):
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    if t.dim() != ndim or not t.is_contiguous():
+        raise ValueError(f"{name} must be a contiguous {ndim}-D tensor")
+
+
+def version() -> int:
+    return lib().wide_version()
+
+
+def num_sms() -> int:
+    return lib().wide_num_sms()
+
+
+def device_status(stream=None) -> None:
+    """Synchronise and raise if a kernel recorded a device-side failure."""
+    _check("wide_device_status", lib().wide_device_status(_stream(stream)))
+
+
+def reorder_masks(mask, perm=None, counts=None, stream=None):
+    """Eq. 7 stable SortDesc per routing column -> (perm [ng, T], counts [ng])."""
+    _need(mask, torch.uint8, "mask", 2)
+    T, ng = mask.shape
+    if perm is None:
+        perm = torch.empty((ng, T), dtype=torch.int32, device=mask.device)
+    if counts is None:
+        counts = torch.empty((ng,), dtype=torch.int32, device=mask.device)
+    _check("wide_reorder_masks", lib().wide_reorder_masks(
+        _ptr(mask), T, ng, _ptr(perm), _ptr(counts), None, 0, _stream(stream)))
+    return perm, counts
+
+
+def gemm_mn_gate_up(X, W_gate, W_up, mask, perm, counts, G, out=None, stream=None):
+    """H = M (.)_G silu(X W_gate^T) * (X W_up^T), bf16 [T, d_ffn]."""
+    _need(X, torch.bfloat16, "X", 2)
+    _need(W_gate, torch.bfloat16, "W_gate", 2)
+    _need(W_up, torch.bfloat16, "W_up", 2)
+    _need(mask, torch.uint8, "mask", 2)
+    T, D = X.shape
+    F = W_gate.shape[0]
+    if out is None:
+        out = torch.empty((T, F), dtype=torch.bfloat16, device=X.device)
+    _check("wide_gemm_mn_gate_up", lib().wide_gemm_mn_gate_up(
+        _ptr(X), _ptr(W_gate), _ptr(W_up), _ptr(mask), _ptr(perm), _ptr(counts),
+        T, D, F, G, _ptr(out), _stream(stream)))
+    return out
+
+
+def gemm_k_workspace_size(T, K, N, G) -> int:
+    return int(lib().wide_gemm_k_workspace_size(T, K, N, G))
+
+
+def gemm_k_down(H, W_down, mask, perm, counts, G, out=None, ws=None, stream=None):
+    """Y = sum over active groups of H[:, K_g] W_down[:, K_g]^T, bf16 [T, d_model]."""
+    _need(H, torch.bfloat16, "H", 2)
+    _need(W_down, torch.bfloat16, "W_down", 2)
+    _need(mask, torch.uint8, "mask", 2)
+    T, F = H.shape
+    D = W_down.shape[0]
+    if out is None:
+        out = torch.empty((T, D), dtype=torch.bfloat16, device=H.device)
+    need = gemm_k_workspace_size(T, F, D, G)
+    if need and ws is None:
+        ws = torch.empty((need,), dtype=torch.uint8, device=H.device)
+    _check("wide_gemm_k_down", lib().wide_gemm_k_down(
+        _ptr(H), _ptr(W_down), _ptr(mask), _ptr(perm), _ptr(counts), T, F, D, G,
+        _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return out
+
+
+def proj_mn(X, W, mask, perm, counts, G, out=None, stream=None):
+    """Y = M (.)_G (X W^T): q_proj over head groups (GEMM-MN)."""
+    _need(X, torch.bfloat16, "X", 2)
+    _need(W, torch.bfloat16, "W", 2)
+    _need(mask, torch.uint8, "mask", 2)
+    T, K = X.shape
+    N = W.shape[0]
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=X.device)
+    _check("wide_proj_mn", lib().wide_proj_mn(
+        _ptr(X), _ptr(W), _ptr(mask), _ptr(perm), _ptr(counts), T, K, N, G,
+        _ptr(out), _stream(stream)))
+    return out
+
+
+def proj_k(A, W, mask, perm, counts, G, out=None, ws=None, stream=None):
+    """Y = sum over active head groups of A[:, K_g] W[:, K_g]^T: o_proj (GEMM-K)."""
+    _need(A, torch.bfloat16, "A", 2)
+    _need(W, torch.bfloat16, "W", 2)
+    _need(mask, torch.uint8, "mask", 2)
+    T, K = A.shape
+    N = W.shape[0]
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=A.device)
+    need = gemm_k_workspace_size(T, K, N, G)
+    if need and ws is None:
+        ws = torch.empty((need,), dtype=torch.uint8, device=A.device)
+    _check("wide_proj_k", lib().wide_proj_k(
+        _ptr(A), _ptr(W), _ptr(mask), _ptr(perm), _ptr(counts), T, K, N, G,
+        _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return out
+
+
+def ffn_forward(X, W_gate, W_up, W_down, mask, G, H=None, Y=None, perm=None, counts=None,
+                stream=None):
+    """Masked FFN of Eq. 3: reorder -> GEMM-MN gate/up (fused SiLU) -> GEMM-K down."""
+    T = X.shape[0]
+    if T > 16 or perm is not None:
+        perm, counts = reorder_masks(mask, perm, counts, stream=stream)
+    H = gemm_mn_gate_up(X, W_gate, W_up, mask, perm, counts, G, out=H, stream=stream)
+    return gemm_k_down(H, W_down, mask, perm, counts, G, out=Y, stream=stream)
+
+
+def ffn_forward_host(X_host, mask_host, W_gate, W_up, W_down, G, Y_host=None, stream=None):
+    """End-to-end call with HOST inputs: copies X and the mask from (pinned) host
+    memory to the device, runs the masked FFN and copies Y back to the host."""
+    dev = W_gate.device
+    X = X_host.to(dev, non_blocking=True)
+    mask = mask_host.to(dev, non_blocking=True)
+    Y = ffn_forward(X, W_gate, W_up, W_down, mask, G, stream=stream)
+    if Y_host is None:
+        Y_host = torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True)
+    Y_host.copy_(Y, non_blocking=True)
+    return Y_host

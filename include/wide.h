@@ -1,0 +1,153 @@
+/*
+ * wide.h -- C ABI of libwide.so: GB300 (sm_103a) kernels for the hot path of
+ * WIDE token-level dynamic width pruning ("WIDE: Boosting Adaptive LLM
+ * Inference via Token-level Dynamic Width Pruning", arXiv 2607.28418).
+ *
+ * Notation (Sec. 3.3): a projection is C = A B^T with A in R^{M x K} (token
+ * rows; batch and sequence flattened into M, called T here), B in R^{N x K}
+ * (nn.Linear weight layout, [out_features, in_features], K contiguous).
+ * A routing mask M in {0,1}^{T x n_groups} (row-major uint8, any nonzero byte
+ * means active) selects, per token, contiguous groups of G channels:
+ *   - GEMM-MN: groups tile the OUTPUT features N (q_proj, gate/up), Eq. 2-3;
+ *   - GEMM-K : groups tile the REDUCTION dimension K (o_proj, down), Eq. 21.
+ *
+ * Conventions shared by every call:
+ *   - All tensor pointers are DEVICE pointers owned by the caller.  bf16
+ *     tensors are passed as their raw 16-bit patterns (uint16_t), row-major
+ *     and densely packed.  Every pointer must be 16-byte aligned.
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream).  Calls only
+ *     enqueue work on it: no host synchronisation, no device-to-host copy, no
+ *     allocation.  Nothing is returned to the host through memory.
+ *   - Shapes: T >= 1; G in {64, 128, 256, 512}; every feature dimension is a
+ *     multiple of 64 and of G where it is grouped.
+ *   - Outputs are fully overwritten (never accumulated into): MN outputs hold
+ *     exact zeros in inactive (token, group) blocks; K outputs of a token with
+ *     no active group are zero.  K calls ignore the values of A inside
+ *     inactive groups (Eq. 21 multiplies them by M).
+ *   - Errors: argument errors are detected on the host before anything is
+ *     launched (WIDE_ERR_INVALID_ARG / WIDE_ERR_UNSUPPORTED).  A failed
+ *     launch returns WIDE_ERR_CUDA.  Kernels never trap: a pipeline wait that
+ *     exceeds its time limit records WIDE_ERR_TIMEOUT in a device status word
+ *     that wide_device_status() reads back.
+ */
+#ifndef WIDE_H
+#define WIDE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    WIDE_OK = 0,
+    WIDE_ERR_INVALID_ARG = 1,  /* null/misaligned pointer, bad shape          */
+    WIDE_ERR_UNSUPPORTED = 2,  /* valid but not implemented (e.g. G = 32)     */
+    WIDE_ERR_WORKSPACE = 3,    /* workspace missing or smaller than required  */
+    WIDE_ERR_CUDA = 4,         /* a CUDA runtime/driver call failed           */
+    WIDE_ERR_TIMEOUT = 5       /* a device-side wait gave up (see above)      */
+} wide_status_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+const char *wide_status_string(int status);
+
+/* Library version, major*10000 + minor*100 + patch. */
+int wide_version(void);
+
+/* Number of SMs the persistent kernels size their grids to (device of the
+ * calling thread); 0 if no device is visible. */
+int wide_num_sms(void);
+
+/*
+ * Mask reordering -- Sec. 3.3 Eq. 7 and App. B Algorithm 1: every routing
+ * column M[:, g] is SortDesc-ed independently, packing the active rows into
+ * a prefix.  The sort is stable: perm[g][0 .. counts[g]) lists the active
+ * rows of group g in ascending order, perm[g][counts[g] .. T) the inactive
+ * rows in ascending order, so M[perm[g][j], g] != 0 exactly when
+ * j < counts[g] (the index identity of App. B).
+ *   mask   : uint8 [T, n_groups] row-major (device)
+ *   perm   : int32 [n_groups, T] group-major (device, written)
+ *   counts : int32 [n_groups]    (device, written)
+ *   ws     : unused, may be NULL (wide_reorder_workspace_size() returns 0)
+ * Bit-exact and deterministic.  T <= 2^31 - 1, 1 <= n_groups <= 65535.
+ */
+wide_status_t wide_reorder_masks(const uint8_t *mask, int T, int n_groups,
+                                 int32_t *perm, int32_t *counts,
+                                 void *ws, size_t ws_bytes, void *stream);
+size_t wide_reorder_workspace_size(int T, int n_groups);
+
+/*
+ * FFN gate/up projection with fused activation -- Sec. 3.1 Eq. 3 (GEMM-MN,
+ * App. B Algorithm 2):
+ *   H[t, f] = M[t, f/G] * silu(X[t,:] . W_gate[f,:]) * (X[t,:] . W_up[f,:])
+ * with silu(a) = a * sigmoid(a), fp32 accumulation, bf16 (RNE) output.
+ *   X        : bf16 [T, d_model]
+ *   W_gate   : bf16 [d_ffn, d_model];  W_up : bf16 [d_ffn, d_model]
+ *   mask     : uint8 [T, d_ffn/G]
+ *   perm, counts : output of wide_reorder_masks() for this mask; may be NULL
+ *              when T <= 16 (the decode path reads the mask directly)
+ *   H        : bf16 [T, d_ffn] (written; inactive blocks are 0)
+ * d_model % 64 == 0, d_ffn % G == 0.
+ */
+wide_status_t wide_gemm_mn_gate_up(const uint16_t *X, const uint16_t *W_gate,
+                                   const uint16_t *W_up, const uint8_t *mask,
+                                   const int32_t *perm, const int32_t *counts,
+                                   int T, int d_model, int d_ffn, int G,
+                                   uint16_t *H, void *stream);
+
+/*
+ * FFN down projection -- Sec. 3.1 Eq. 3 / App. B Eq. 21 (GEMM-K):
+ *   Y[t, n] = sum_g M[t,g] sum_{f in [gG, (g+1)G)} H[t,f] * W_down[n,f]
+ *   H      : bf16 [T, d_ffn]   (values inside inactive groups are ignored)
+ *   W_down : bf16 [d_model, d_ffn]
+ *   mask   : uint8 [T, d_ffn/G]; perm/counts as above (may be NULL)
+ *   Y      : bf16 [T, d_model] (written)
+ *   ws     : device workspace of at least
+ *            wide_gemm_k_workspace_size(T, d_ffn, d_model, G) bytes
+ *            (may be NULL when that size is 0)
+ * fp32 accumulation in ascending group order; deterministic.
+ */
+wide_status_t wide_gemm_k_down(const uint16_t *H, const uint16_t *W_down,
+                               const uint8_t *mask, const int32_t *perm,
+                               const int32_t *counts, int T, int d_ffn,
+                               int d_model, int G, uint16_t *Y, void *ws,
+                               size_t ws_bytes, void *stream);
+
+/*
+ * Plain GEMM-MN (q_proj over GQA head groups, Sec. 3.1 Eq. 2; the M-axis
+ * case is n_groups = N/G = 1, Sec. 3.3):
+ *   Y[t, n] = M[t, n/G] * sum_k X[t,k] W[n,k]
+ *   X : bf16 [T, K];  W : bf16 [N, K];  mask : uint8 [T, N/G];  Y : bf16 [T, N]
+ */
+wide_status_t wide_proj_mn(const uint16_t *X, const uint16_t *W,
+                           const uint8_t *mask, const int32_t *perm,
+                           const int32_t *counts, int T, int K, int N, int G,
+                           uint16_t *Y, void *stream);
+
+/*
+ * Plain GEMM-K (o_proj over GQA head groups, Sec. 3.1 Eq. 2; App. B Eq. 21):
+ *   Y[t, n] = sum_g M[t,g] sum_{k in [gG, (g+1)G)} A[t,k] W[n,k]
+ *   A : bf16 [T, K];  W : bf16 [N, K];  mask : uint8 [T, K/G];  Y : bf16 [T, N]
+ *   ws as for wide_gemm_k_down.
+ */
+wide_status_t wide_proj_k(const uint16_t *A, const uint16_t *W,
+                          const uint8_t *mask, const int32_t *perm,
+                          const int32_t *counts, int T, int K, int N, int G,
+                          uint16_t *Y, void *ws, size_t ws_bytes, void *stream);
+
+/* Workspace bytes a GEMM-K call needs for these sizes (0 = none). */
+size_t wide_gemm_k_workspace_size(int T, int K, int N, int G);
+
+/*
+ * Device status word: synchronises `stream`, returns WIDE_OK or the first
+ * device-side failure recorded since the last call (WIDE_ERR_TIMEOUT), and
+ * clears it.  This is the only call that synchronises.
+ */
+wide_status_t wide_device_status(void *stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WIDE_H */
