@@ -4,6 +4,8 @@
 // word.  No call allocates, frees or synchronises (except wide_device_status).
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
+#include <cstring>
 #include <mutex>
 
 #include "../../include/wide.h"
@@ -28,6 +30,16 @@ std::mutex g_mutex;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 int g_num_sms[kMaxDevices] = {0};
 int *g_status_ptr[kMaxDevices] = {nullptr};
+
+// A-operand gather used by GEMM-MN prefill tiles.
+wide::Gather mn_gather() {
+    static const wide::Gather g = [] {
+        const char *v = std::getenv("WIDE_MN_GATHER");
+        return (v != nullptr && std::strcmp(v, "cpasync") == 0) ? wide::Gather::kCpAsync
+                                                                 : wide::Gather::kTma4;
+    }();
+    return g;
+}
 
 wide_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? WIDE_OK : WIDE_ERR_CUDA; }
 
@@ -139,8 +151,9 @@ wide_status_t run_mn(wide::MNMode mode, const uint16_t *X, const uint16_t *W0,
     if ((st = encode_bf16_2d(&tmA, X, T, K, 1)) != WIDE_OK) return st;
     if ((st = encode_bf16_2d(&tmB0, W0, N, K, bn)) != WIDE_OK) return st;
     if ((st = encode_bf16_2d(&tmB1, gate_up ? W1 : W0, N, K, bn)) != WIDE_OK) return st;
-    wide::MNArgs a{perm, counts, out, T, K, N, G, ctx.status};
-    return from_cuda(wide::launch_gemm_mn(mode, bn, tmA, tmB0, tmB1, a, ctx.num_sms, s));
+    wide::MNArgs a{X, perm, counts, out, T, K, N, G, ctx.status};
+    return from_cuda(
+        wide::launch_gemm_mn(mode, mn_gather(), bn, tmA, tmB0, tmB1, a, ctx.num_sms, s));
 }
 
 wide_status_t run_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask, int T, int K,

@@ -9,11 +9,15 @@
 // perm[g][0 .. counts[g]).
 //
 // GB300 design (one persistent CTA per SM, 6 warps):
-//   warp 0      TMA producer: A rows are gathered by token index with
-//               cp.async.bulk.tensor tile::gather4 (4 rows per instruction,
-//               one instruction per lane); only the packets that hold active
-//               rows are issued (the l=1 predicate of Eq. 20).  The weight
-//               tile of the group streams densely with a tiled TMA load.
+//   warp 0      TMA producer of the weight tile of the group (dense, tiled
+//               TMA) and, in the kTma4 gather mode, of the gathered A rows
+//               (cp.async.bulk.tensor tile::gather4: 4 rows per instruction,
+//               one instruction per lane).
+//   warps 6..9  (kCpAsync gather mode) gather the A rows with 16-byte
+//               cp.async copies written straight into the 128-byte-swizzled
+//               layout, one 128-byte row segment per 8 lanes.
+//               In both modes only the packets that hold active rows are
+//               copied (the l=1 predicate of Eq. 20).
 //   warp 1      TMEM owner and single-thread tcgen05.mma issuer
 //               (M = 128 gathered rows, N = 2 x 128 for gate/up, K = 16 per
 //               instruction, fp32 accumulators in TMEM, double buffered).
@@ -32,7 +36,12 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle row of bf16
-constexpr int kThreads = 192;
+constexpr int kBaseThreads = 192;  // producer, MMA, 4 epilogue warps
+constexpr int kGatherWarps = 4;    // extra warps of the kCpAsync gather
+
+__host__ __device__ constexpr int mn_threads(Gather g) {
+    return g == Gather::kCpAsync ? kBaseThreads + 32 * kGatherWarps : kBaseThreads;
+}
 constexpr int kSmemBudget = 225 * 1024;
 
 template <MNMode MODE, int BN_OP>
@@ -120,11 +129,13 @@ __device__ __forceinline__ float silu_mul(float gate, float up) {
     return __fdividef(gate, 1.0f + __expf(-gate)) * up;
 }
 
-template <MNMode MODE, int BN_OP>
-__global__ void __launch_bounds__(kThreads, 1)
+template <MNMode MODE, int BN_OP, Gather GATHER>
+__global__ void __launch_bounds__(mn_threads(GATHER), 1)
     gemm_mn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
                    const __grid_constant__ CUtensorMap tmB1, const MNArgs args) {
     using C = Cfg<MODE, BN_OP>;
+    constexpr int kThreads = mn_threads(GATHER);
+    constexpr bool kCp = GATHER == Gather::kCpAsync;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -156,7 +167,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full[s], 1);
+            // kCpAsync: + one arrival per gather thread once its copies landed
+            mbar_init(&full[s], kCp ? 1 + 32 * kGatherWarps : 1);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -206,13 +218,15 @@ __global__ void __launch_bounds__(kThreads, 1)
             const int c = sch.counts[it.g];
             const int row0 = it.m * BM;
             const int rows_valid = min(BM, c - row0);
-            const int n_g4 = (rows_valid + 3) >> 2;
-            int r[4];
-            const int pad = ld_nc_s32(pg + row0);
+            const int n_g4 = kCp ? 0 : (rows_valid + 3) >> 2;
+            int r[4] = {0, 0, 0, 0};
+            if (!kCp) {
+                const int pad = ld_nc_s32(pg + row0);
 #pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const int rr = 4 * lane + j;
-                r[j] = rr < rows_valid ? ld_nc_s32(pg + row0 + rr) : pad;
+                for (int j = 0; j < 4; ++j) {
+                    const int rr = 4 * lane + j;
+                    r[j] = rr < rows_valid ? ld_nc_s32(pg + row0 + rr) : pad;
+                }
             }
             const uint32_t bytes = static_cast<uint32_t>(n_g4 * 4 * BK * 2 + C::B_BYTES);
             const int nrow = it.g * args.G + it.ns * BN_OP;
@@ -225,7 +239,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 uint8_t *sb = sa + C::A_BYTES;
                 if (lane == 0) mbar_arrive_expect_tx(&full[stage], bytes);
                 __syncwarp();
-                if (lane < n_g4)
+                if (!kCp && lane < n_g4)
                     tma_gather4(sa + lane * 4 * BK * 2, &tmA, &full[stage], kb * BK, r[0], r[1], r[2], r[3]);
                 if (lane == 0) {
                     tma_load_2d(sb, &tmB0, &full[stage], kb * BK, nrow);
@@ -276,6 +290,59 @@ __global__ void __launch_bounds__(kThreads, 1)
             mbar_wait(final_bar, 0, args.status);
         }
         __syncwarp();
+    } else if (kCp && warp >= 6) {
+        // ===================== cp.async row gather (warps 6..9) =====================
+        // Warp gw owns rows 32*gw .. 32*gw+31 of the A tile; one instruction
+        // copies 4 rows x 128 bytes (8 lanes per row, 16 bytes per lane) into
+        // the 128-byte-swizzled layout the UMMA descriptor expects.  Copies of
+        // a stage are completed, made visible to the tensor core's async
+        // proxy and announced on full[stage] with a lag of L stages, so L
+        // stages of copies stay in flight per thread.
+        constexpr int L = C::STAGES - 1;
+        const int gw = warp - 6;
+        const int sub = lane >> 3, chunk = lane & 7;
+        int stage = 0;
+        uint32_t phase = 0;
+        int pending = 0;  // committed groups not yet announced (consecutive stages)
+        int last_stage = 0;
+        for (int i = blockIdx.x; i < sch.n_total && !*s_abort; i += gridDim.x) {
+            const Item it = decode_item(sch, i);
+            if (it.zero) continue;
+            const int32_t *pg = args.perm + static_cast<size_t>(it.g) * T;
+            const int rows_valid = min(BM, sch.counts[it.g] - it.m * BM);
+            const int my_row = 32 * gw + lane;
+            const int my_tok = my_row < rows_valid ? ld_nc_s32(pg + it.m * BM + my_row) : -1;
+            for (int kb = 0; kb < k_blocks; ++kb) {
+                int ok = 1;
+                if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, args.status);
+                ok = __shfl_sync(0xffffffffu, ok, 0);
+                if (!ok) { *s_abort = 1; break; }
+                const uint32_t sa = smem_u32(stages + stage * C::STAGE_BYTES);
+#pragma unroll
+                for (int q = 0; q < 8; ++q) {
+                    const int rl = 4 * q + sub;  // row inside this warp's 32
+                    const int tok = __shfl_sync(0xffffffffu, my_tok, rl);
+                    const int row = 32 * gw + rl;
+                    if (tok >= 0) {
+                        const uint16_t *src = args.a_rows + static_cast<size_t>(tok) * args.K + kb * BK + chunk * 8;
+                        cp_async16(sa + row * 128 + ((chunk ^ (row & 7)) << 4), src);
+                    }
+                }
+                cp_async_commit();
+                last_stage = stage;
+                if (++pending > L) {
+                    cp_async_wait<L>();
+                    fence_proxy_async_smem();
+                    mbar_arrive(&full[(stage + C::STAGES - L) % C::STAGES]);
+                    --pending;
+                }
+                if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
+            }
+        }
+        cp_async_wait<0>();
+        fence_proxy_async_smem();
+        for (; pending > 0; --pending)
+            mbar_arrive(&full[(last_stage + C::STAGES - (pending - 1)) % C::STAGES]);
     } else {
         // ===================== epilogue (warps 2..5) =====================
         const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
@@ -346,28 +413,36 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <MNMode MODE, int BN_OP>
-cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB0, const CUtensorMap &tmB1,
+template <MNMode MODE, int BN_OP, Gather GATHER>
+cudaError_t launch_g(const CUtensorMap &tmA, const CUtensorMap &tmB0, const CUtensorMap &tmB1,
                      const MNArgs &a, int num_sms, cudaStream_t s) {
     using C = Cfg<MODE, BN_OP>;
-    auto kern = gemm_mn_kernel<MODE, BN_OP>;
+    auto kern = gemm_mn_kernel<MODE, BN_OP, GATHER>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<num_sms, kThreads, C::SMEM_BYTES, s>>>(tmA, tmB0, tmB1, a);
+    kern<<<num_sms, mn_threads(GATHER), C::SMEM_BYTES, s>>>(tmA, tmB0, tmB1, a);
     return cudaGetLastError();
+}
+
+template <MNMode MODE, int BN_OP>
+cudaError_t launch_t(Gather g, const CUtensorMap &tmA, const CUtensorMap &tmB0,
+                     const CUtensorMap &tmB1, const MNArgs &a, int num_sms, cudaStream_t s) {
+    if (g == Gather::kCpAsync) return launch_g<MODE, BN_OP, Gather::kCpAsync>(tmA, tmB0, tmB1, a, num_sms, s);
+    return launch_g<MODE, BN_OP, Gather::kTma4>(tmA, tmB0, tmB1, a, num_sms, s);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_mn(MNMode mode, int bn, const CUtensorMap &tmA, const CUtensorMap &tmB0,
-                           const CUtensorMap &tmB1, const MNArgs &a, int num_sms, cudaStream_t s) {
+cudaError_t launch_gemm_mn(MNMode mode, Gather g, int bn, const CUtensorMap &tmA,
+                           const CUtensorMap &tmB0, const CUtensorMap &tmB1, const MNArgs &a,
+                           int num_sms, cudaStream_t s) {
     if (mode == MNMode::kGateUp) {
-        if (bn == 128) return launch_t<MNMode::kGateUp, 128>(tmA, tmB0, tmB1, a, num_sms, s);
-        if (bn == 64) return launch_t<MNMode::kGateUp, 64>(tmA, tmB0, tmB1, a, num_sms, s);
+        if (bn == 128) return launch_t<MNMode::kGateUp, 128>(g, tmA, tmB0, tmB1, a, num_sms, s);
+        if (bn == 64) return launch_t<MNMode::kGateUp, 64>(g, tmA, tmB0, tmB1, a, num_sms, s);
     } else {
-        if (bn == 256) return launch_t<MNMode::kPlain, 256>(tmA, tmB0, tmB1, a, num_sms, s);
-        if (bn == 128) return launch_t<MNMode::kPlain, 128>(tmA, tmB0, tmB1, a, num_sms, s);
-        if (bn == 64) return launch_t<MNMode::kPlain, 64>(tmA, tmB0, tmB1, a, num_sms, s);
+        if (bn == 256) return launch_t<MNMode::kPlain, 256>(g, tmA, tmB0, tmB1, a, num_sms, s);
+        if (bn == 128) return launch_t<MNMode::kPlain, 128>(g, tmA, tmB0, tmB1, a, num_sms, s);
+        if (bn == 64) return launch_t<MNMode::kPlain, 64>(g, tmA, tmB0, tmB1, a, num_sms, s);
     }
     return cudaErrorInvalidValue;
 }
