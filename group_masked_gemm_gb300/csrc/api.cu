@@ -4,8 +4,6 @@
 // word.  No call allocates, frees or synchronises (except wide_device_status).
 #include <cudaTypedefs.h>
 
-#include <cstdlib>
-#include <cstring>
 #include <mutex>
 
 #include "../../include/wide.h"
@@ -30,16 +28,6 @@ std::mutex g_mutex;
 PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
 int g_num_sms[kMaxDevices] = {0};
 int *g_status_ptr[kMaxDevices] = {nullptr};
-
-// A-operand gather used by GEMM-MN prefill tiles.
-wide::Gather mn_gather() {
-    static const wide::Gather g = [] {
-        const char *v = std::getenv("WIDE_MN_GATHER");
-        return (v != nullptr && std::strcmp(v, "cpasync") == 0) ? wide::Gather::kCpAsync
-                                                                 : wide::Gather::kTma4;
-    }();
-    return g;
-}
 
 wide_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? WIDE_OK : WIDE_ERR_CUDA; }
 
@@ -147,13 +135,17 @@ wide_status_t run_mn(wide::MNMode mode, const uint16_t *X, const uint16_t *W0,
     }
     if (perm == nullptr || counts == nullptr) return WIDE_ERR_INVALID_ARG;
     const int bn = gate_up ? (G == 64 ? 64 : 128) : (G == 64 ? 64 : G == 128 ? 128 : 256);
-    CUtensorMap tmA, tmB0, tmB1;
-    if ((st = encode_bf16_2d(&tmA, X, T, K, 1)) != WIDE_OK) return st;
+    CUtensorMap tmB0, tmB1;
     if ((st = encode_bf16_2d(&tmB0, W0, N, K, bn)) != WIDE_OK) return st;
     if ((st = encode_bf16_2d(&tmB1, gate_up ? W1 : W0, N, K, bn)) != WIDE_OK) return st;
-    wide::MNArgs a{X, perm, counts, out, T, K, N, G, ctx.status};
-    return from_cuda(
-        wide::launch_gemm_mn(mode, mn_gather(), bn, tmA, tmB0, tmB1, a, ctx.num_sms, s));
+    // Token bands of the tile order: keep one band of X (~32 MiB) resident in L2.
+    const int ng = N / G;
+    const long long x_bytes = static_cast<long long>(T) * K * 2;
+    int bands = static_cast<int>((x_bytes + (32ll << 20) - 1) / (32ll << 20));
+    bands = bands < 1 ? 1 : bands > 16 ? 16 : bands;
+    while (bands > 1 && bands * ng > wide::kMaxGroups) --bands;
+    wide::MNArgs a{X, perm, counts, out, T, K, N, G, bands, ctx.status};
+    return from_cuda(wide::launch_gemm_mn(mode, bn, tmB0, tmB1, a, ctx.num_sms, s));
 }
 
 wide_status_t run_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask, int T, int K,

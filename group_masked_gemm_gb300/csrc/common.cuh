@@ -1,5 +1,5 @@
 // common.cuh -- device helpers shared by the libwide kernels (sm_103a only):
-// mbarrier waits with a time limit, TMA tile / gather4 loads, tcgen05 MMA,
+// mbarrier waits with a time limit, TMA tile loads, cp.async, tcgen05 MMA,
 // TMEM allocation and loads, UMMA shared-memory and instruction descriptors.
 #pragma once
 
@@ -91,29 +91,19 @@ __device__ __forceinline__ void tma_load_2d(void *dst, const CUtensorMap *m, uin
         : "memory");
 }
 
-// Row gather: four rows r0..r3 (one-row-high box) starting at column x,
-// written as four consecutive box rows at dst.
-__device__ __forceinline__ void tma_gather4(void *dst, const CUtensorMap *m, uint64_t *bar,
-                                            int x, int r0, int r1, int r2, int r3) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile::gather4.mbarrier::complete_tx::bytes"
-        " [%0], [%1, {%2, %3, %4, %5, %6}], [%7];" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(m)), "r"(x), "r"(r0), "r"(r1), "r"(r2), "r"(r3),
-        "r"(smem_u32(bar))
-        : "memory");
-}
-
 // ---------------------------------------------------------------- cp.async --
 // 16-byte global -> shared copy (L2 only), completion tracked per thread.
 __device__ __forceinline__ void cp_async16(uint32_t dst_smem, const void *src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst_smem), "l"(src) : "memory");
 }
-__device__ __forceinline__ void cp_async_commit() {
-    asm volatile("cp.async.commit_group;" ::: "memory");
+// Arrive (without a pending-count increment) on an mbarrier once all of this
+// thread's prior cp.async copies have landed.
+__device__ __forceinline__ void cp_async_mbar_arrive_noinc(uint64_t *bar) {
+    asm volatile("cp.async.mbarrier.arrive.noinc.shared::cta.b64 [%0];" ::"r"(smem_u32(bar))
+                 : "memory");
 }
-template <int N>
-__device__ __forceinline__ void cp_async_wait() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.wait_all;" ::: "memory");
 }
 // Make generic-proxy writes to shared memory visible to the async proxy
 // (tensor-core operand reads).
@@ -246,6 +236,15 @@ __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
 __device__ __forceinline__ void st_global_v4(void *p, uint32_t a, uint32_t b, uint32_t c,
                                              uint32_t d) {
     asm volatile("st.global.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
+                 "r"(d)
+                 : "memory");
+}
+
+// Streaming store: the line is written once and should be evicted first, so
+// outputs do not push reused operands out of L2.
+__device__ __forceinline__ void st_global_cs_v4(void *p, uint32_t a, uint32_t b, uint32_t c,
+                                                uint32_t d) {
+    asm volatile("st.global.cs.v4.b32 [%0], {%1, %2, %3, %4};" ::"l"(p), "r"(a), "r"(b), "r"(c),
                  "r"(d)
                  : "memory");
 }

@@ -48,11 +48,20 @@ struct KCfg {
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
+// Mask buffer b (of 2) inside the mask area: lane masks [ng][4], the live
+// group list [ng] and its length.
 struct MaskBuf {
     uint32_t *lanes;  // [ng][4] disable-output-lane words
     int *live;        // [ng] live groups, ascending
     int *n_live;
 };
+
+template <int BUF_BYTES>
+__device__ __forceinline__ MaskBuf mask_buf(uint8_t *area, int b) {
+    uint8_t *base = area + b * BUF_BYTES;
+    return MaskBuf{reinterpret_cast<uint32_t *>(base), reinterpret_cast<int *>(base + kMaxKGroups * 16),
+                   reinterpret_cast<int *>(base + kMaxKGroups * 20)};
+}
 
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -64,13 +73,6 @@ __global__ void __launch_bounds__(kThreads, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     uint8_t *stages = smem;
     uint8_t *mask_area = smem + C::STAGES * C::STAGE_BYTES;
-    MaskBuf mb[2];
-    for (int b = 0; b < 2; ++b) {
-        uint8_t *base = mask_area + b * C::MASK_BUF_BYTES;
-        mb[b].lanes = reinterpret_cast<uint32_t *>(base);
-        mb[b].live = reinterpret_cast<int *>(base + kMaxKGroups * 16);
-        mb[b].n_live = reinterpret_cast<int *>(base + kMaxKGroups * 20);
-    }
     uint64_t *bars = reinterpret_cast<uint64_t *>(mask_area + 2 * C::MASK_BUF_BYTES);
     uint64_t *full = bars;
     uint64_t *empty = bars + C::STAGES;
@@ -143,6 +145,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) ok = mbar_wait(&mempty[b], bphase ^ 1u, args.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { *s_abort = 1; break; }
+            const MaskBuf mbuf = mask_buf<C::MASK_BUF_BYTES>(mask_area, b);
             int n_live = 0;
             constexpr int kU = 8;  // groups per batch of independent loads
             for (int g0 = 0; g0 < ng; g0 += kU) {
@@ -163,14 +166,17 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int q = 0; q < 4; ++q) w[q] = __ballot_sync(0xffffffffu, v[u][q] != 0);
                     const bool live = (w[0] | w[1] | w[2] | w[3]) != 0u;
-                    if (lane < 4) mb[b].lanes[g * 4 + lane] = ~w[lane];
+                    if (lane < 4) {
+                        const uint32_t wl = lane == 0 ? w[0] : lane == 1 ? w[1] : lane == 2 ? w[2] : w[3];
+                        mbuf.lanes[g * 4 + lane] = ~wl;
+                    }
                     if (live) {
-                        if (lane == 0) mb[b].live[n_live] = g;
+                        if (lane == 0) mbuf.live[n_live] = g;
                         ++n_live;
                     }
                 }
             }
-            if (lane == 0) *mb[b].n_live = n_live;
+            if (lane == 0) *mbuf.n_live = n_live;
             __threadfence_block();
             __syncwarp();
             if (lane == 0) mbar_arrive(&mfull[b]);  // release semantics publish the buffer
@@ -189,9 +195,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) ok = mbar_wait(&mfull[b], bphase, args.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { *s_abort = 1; break; }
-            const int n_live = *mb[b].n_live;
+            const MaskBuf mbuf = mask_buf<C::MASK_BUF_BYTES>(mask_area, b);
+            const int n_live = *mbuf.n_live;
             for (int li = 0; li < n_live && ok; ++li) {
-                const int g = mb[b].live[li];
+                const int g = mbuf.live[li];
                 for (int kb = 0; kb < kb_per_group; ++kb) {
                     if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, args.status);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -231,12 +238,13 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, args.status)) { *s_abort = 1; break; }
                 tc_fence_after();
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
-                const int n_live = *mb[b].n_live;
+                const MaskBuf mbuf = mask_buf<C::MASK_BUF_BYTES>(mask_area, b);
+                const int n_live = *mbuf.n_live;
                 bool ok = true;
                 for (int li = 0; li < n_live && ok; ++li) {
-                    const int g = mb[b].live[li];
-                    const uint32_t l0 = mb[b].lanes[g * 4 + 0], l1 = mb[b].lanes[g * 4 + 1];
-                    const uint32_t l2 = mb[b].lanes[g * 4 + 2], l3 = mb[b].lanes[g * 4 + 3];
+                    const int g = mbuf.live[li];
+                    const uint32_t l0 = mbuf.lanes[g * 4 + 0], l1 = mbuf.lanes[g * 4 + 1];
+                    const uint32_t l2 = mbuf.lanes[g * 4 + 2], l3 = mbuf.lanes[g * 4 + 3];
                     for (int kb = 0; kb < kb_per_group; ++kb) {
                         if (!mbar_wait(&full[stage], phase, args.status)) { ok = false; break; }
                         tc_fence_after();
@@ -290,7 +298,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (t < T) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        st_global_v4(dst + cb + 8 * q,
+                        st_global_cs_v4(dst + cb + 8 * q,
                                      pack_bf16x2(__uint_as_float(yr[8 * q + 0]), __uint_as_float(yr[8 * q + 1])),
                                      pack_bf16x2(__uint_as_float(yr[8 * q + 2]), __uint_as_float(yr[8 * q + 3])),
                                      pack_bf16x2(__uint_as_float(yr[8 * q + 4]), __uint_as_float(yr[8 * q + 5])),

@@ -8,16 +8,18 @@
 // reordered order of each routing column: the active tokens of group g are
 // perm[g][0 .. counts[g]).
 //
-// GB300 design (one persistent CTA per SM, 6 warps):
+// GB300 design (one persistent CTA per SM, 10 warps):
 //   warp 0      TMA producer of the weight tile of the group (dense, tiled
-//               TMA) and, in the kTma4 gather mode, of the gathered A rows
-//               (cp.async.bulk.tensor tile::gather4: 4 rows per instruction,
-//               one instruction per lane).
-//   warps 6..9  (kCpAsync gather mode) gather the A rows with 16-byte
-//               cp.async copies written straight into the 128-byte-swizzled
-//               layout, one 128-byte row segment per 8 lanes.
-//               In both modes only the packets that hold active rows are
-//               copied (the l=1 predicate of Eq. 20).
+//               TMA, 128-byte swizzle).
+//   warps 6..9  gather the A rows (token rows picked through perm) with
+//               16-byte cp.async copies written straight into the
+//               128-byte-swizzled layout the UMMA descriptor expects, one
+//               128-byte row segment per 8 lanes; only the rows that hold
+//               active tokens are copied (the l=1 predicate of Eq. 20).
+//               Measured on GB300, the TMA row gather (tile::gather4) issues
+//               at ~80 clocks per 4-row instruction whichever lanes issue it,
+//               ~6 B/clk per SM against the ~58 B/clk the MMA consumes, so the
+//               gather goes through the load/store path instead.
 //   warp 1      TMEM owner and single-thread tcgen05.mma issuer
 //               (M = 128 gathered rows, N = 2 x 128 for gate/up, K = 16 per
 //               instruction, fp32 accumulators in TMEM, double buffered).
@@ -27,7 +29,12 @@
 // The work list is built in shared memory from counts[]: a tile of group g
 // exists only for row offsets below counts[g] (the l=0 CTA-level predicate
 // becomes "never scheduled"), followed by "zero tiles" that write the exact
-// zeros of the inactive (token, group) blocks.
+// zeros of the inactive (token, group) blocks.  Compute tiles are ordered by
+// (token band, group, tile): each group's tiles are split into `bands`
+// consecutive ranges, and since a group's active tokens are sorted, range b
+// of every group covers about the same band of token rows.  CTAs running at
+// the same time then share one band of X (sized to stay resident in L2) and
+// the weights of a few groups, instead of sweeping all of X for each group.
 #include "common.cuh"
 #include "internal.h"
 
@@ -36,12 +43,8 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;  // one 128-byte swizzle row of bf16
-constexpr int kBaseThreads = 192;  // producer, MMA, 4 epilogue warps
-constexpr int kGatherWarps = 4;    // extra warps of the kCpAsync gather
-
-__host__ __device__ constexpr int mn_threads(Gather g) {
-    return g == Gather::kCpAsync ? kBaseThreads + 32 * kGatherWarps : kBaseThreads;
-}
+constexpr int kGatherWarps = 4;                    // A-row gather warps 6..9
+constexpr int kThreads = 32 * (6 + kGatherWarps);  // producer, MMA, 4 epilogue, 4 gather
 constexpr int kSmemBudget = 225 * 1024;
 
 template <MNMode MODE, int BN_OP>
@@ -64,11 +67,16 @@ struct Cfg {
 };
 
 struct Sched {
-    int *cpre;    // [ng+1] prefix of compute items per group
+    int *cpre;    // [bands*ng+1] prefix of compute items per (band, group)
     int *zpre;    // [ng+1] prefix of zero items per group
     int *counts;  // [ng]
-    int ng, nsub, n_compute, n_total;
+    int ng, nsub, bands, n_compute, n_total;
 };
+
+// First tile of band b for a group with mt tiles: ceil(b * mt / bands).
+__device__ __forceinline__ int band_lo(int b, int mt, int bands) {
+    return (b * mt + bands - 1) / bands;
+}
 
 struct Item {
     int g, m, ns;  // group, 128-row tile of the reordered column, N sub-tile
@@ -88,10 +96,14 @@ __device__ __forceinline__ int upper_group(const int *pre, int ng, int i) {
 __device__ __forceinline__ Item decode_item(const Sched &s, int i) {
     Item it;
     if (i < s.n_compute) {
-        it.g = upper_group(s.cpre, s.ng, i);
-        const int local = i - s.cpre[it.g];
-        it.m = local / s.nsub;
-        it.ns = local - it.m * s.nsub;
+        const int e = upper_group(s.cpre, s.bands * s.ng, i);  // entry (band, group)
+        const int b = e / s.ng;
+        it.g = e - b * s.ng;
+        const int local = i - s.cpre[e];
+        const int mt = (s.counts[it.g] + BM - 1) / BM;
+        const int q = local / s.nsub;
+        it.m = band_lo(b, mt, s.bands) + q;
+        it.ns = local - q * s.nsub;
         it.zero = false;
     } else {
         const int zi = i - s.n_compute;
@@ -129,13 +141,11 @@ __device__ __forceinline__ float silu_mul(float gate, float up) {
     return __fdividef(gate, 1.0f + __expf(-gate)) * up;
 }
 
-template <MNMode MODE, int BN_OP, Gather GATHER>
-__global__ void __launch_bounds__(mn_threads(GATHER), 1)
-    gemm_mn_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB0,
-                   const __grid_constant__ CUtensorMap tmB1, const MNArgs args) {
+template <MNMode MODE, int BN_OP>
+__global__ void __launch_bounds__(kThreads, 1)
+    gemm_mn_kernel(const __grid_constant__ CUtensorMap tmB0, const __grid_constant__ CUtensorMap tmB1,
+                   const MNArgs args) {
     using C = Cfg<MODE, BN_OP>;
-    constexpr int kThreads = mn_threads(GATHER);
-    constexpr bool kCp = GATHER == Gather::kCpAsync;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -157,18 +167,21 @@ __global__ void __launch_bounds__(mn_threads(GATHER), 1)
     const int ng = args.n_out / args.G;
 
     // ---- schedule: tiles of each group exist only below counts[g] ---------
+    const int bands = args.bands;
+    const int nsub = args.G / BN_OP;
     for (int g = threadIdx.x; g < ng; g += kThreads) {
         const int c = ld_nc_s32(args.counts + g);
         s_counts[g] = c;
         const int mt = (c + BM - 1) / BM;
         const int covered = mt * BM;
-        s_cpre[g + 1] = mt * (args.G / BN_OP);
         s_zpre[g + 1] = covered < T ? (T - covered + BM - 1) / BM : 0;
+        for (int b = 0; b < bands; ++b)
+            s_cpre[b * ng + g + 1] = (band_lo(b + 1, mt, bands) - band_lo(b, mt, bands)) * nsub;
     }
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
-            // kCpAsync: + one arrival per gather thread once its copies landed
-            mbar_init(&full[s], kCp ? 1 + 32 * kGatherWarps : 1);
+            // producer's expect_tx arrival + one per gather thread once its copies landed
+            mbar_init(&full[s], 1 + 32 * kGatherWarps);
             mbar_init(&empty[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
@@ -180,7 +193,6 @@ __global__ void __launch_bounds__(mn_threads(GATHER), 1)
         fence_barrier_init();
     }
     if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmA);
         prefetch_tmap(&tmB0);
         if (MODE == MNMode::kGateUp) prefetch_tmap(&tmB1);
     }
@@ -189,7 +201,7 @@ __global__ void __launch_bounds__(mn_threads(GATHER), 1)
         tmem_relinquish();
     }
     __syncthreads();
-    if (warp == 0) warp_prefix(s_cpre, ng);
+    if (warp == 0) warp_prefix(s_cpre, bands * ng);
     if (warp == 1) warp_prefix(s_zpre, ng);
     tc_fence_before();
     __syncthreads();
@@ -200,9 +212,10 @@ __global__ void __launch_bounds__(mn_threads(GATHER), 1)
     sch.zpre = s_zpre;
     sch.counts = s_counts;
     sch.ng = ng;
-    sch.nsub = args.G / BN_OP;
-    sch.n_compute = s_cpre[ng];
-    sch.n_total = s_cpre[ng] + s_zpre[ng];
+    sch.nsub = nsub;
+    sch.bands = bands;
+    sch.n_compute = s_cpre[bands * ng];
+    sch.n_total = sch.n_compute + s_zpre[ng];
     const uint32_t tmem_base = *s_tmem;
     const int k_blocks = args.K / BK;
 
@@ -214,33 +227,15 @@ __global__ void __launch_bounds__(mn_threads(GATHER), 1)
         for (int i = blockIdx.x; i < sch.n_total && !*s_abort; i += gridDim.x) {
             const Item it = decode_item(sch, i);
             if (it.zero) continue;
-            const int32_t *pg = args.perm + static_cast<size_t>(it.g) * T;
-            const int c = sch.counts[it.g];
-            const int row0 = it.m * BM;
-            const int rows_valid = min(BM, c - row0);
-            const int n_g4 = kCp ? 0 : (rows_valid + 3) >> 2;
-            int r[4] = {0, 0, 0, 0};
-            if (!kCp) {
-                const int pad = ld_nc_s32(pg + row0);
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    const int rr = 4 * lane + j;
-                    r[j] = rr < rows_valid ? ld_nc_s32(pg + row0 + rr) : pad;
-                }
-            }
-            const uint32_t bytes = static_cast<uint32_t>(n_g4 * 4 * BK * 2 + C::B_BYTES);
+            const uint32_t bytes = static_cast<uint32_t>(C::B_BYTES);
             const int nrow = it.g * args.G + it.ns * BN_OP;
             for (int kb = 0; kb < k_blocks; ++kb) {
                 int ok = 1;
                 if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, args.status);
                 ok = __shfl_sync(0xffffffffu, ok, 0);
                 if (!ok) { *s_abort = 1; break; }
-                uint8_t *sa = stages + stage * C::STAGE_BYTES;
-                uint8_t *sb = sa + C::A_BYTES;
+                uint8_t *sb = stages + stage * C::STAGE_BYTES + C::A_BYTES;
                 if (lane == 0) mbar_arrive_expect_tx(&full[stage], bytes);
-                __syncwarp();
-                if (!kCp && lane < n_g4)
-                    tma_gather4(sa + lane * 4 * BK * 2, &tmA, &full[stage], kb * BK, r[0], r[1], r[2], r[3]);
                 if (lane == 0) {
                     tma_load_2d(sb, &tmB0, &full[stage], kb * BK, nrow);
                     if (MODE == MNMode::kGateUp)
@@ -272,6 +267,7 @@ __global__ void __launch_bounds__(mn_threads(GATHER), 1)
                 bool ok = true;
                 for (int kb = 0; kb < k_blocks; ++kb) {
                     if (!mbar_wait(&full[stage], phase, args.status)) { ok = false; break; }
+                    fence_proxy_async_smem();  // A rows were written by cp.async (generic proxy)
                     tc_fence_after();
                     const uint32_t a0 = smem_u32(stages + stage * C::STAGE_BYTES);
                     const uint32_t b0 = a0 + C::A_BYTES;
@@ -290,21 +286,19 @@ __global__ void __launch_bounds__(mn_threads(GATHER), 1)
             mbar_wait(final_bar, 0, args.status);
         }
         __syncwarp();
-    } else if (kCp && warp >= 6) {
+    } else if (warp >= 6) {
         // ===================== cp.async row gather (warps 6..9) =====================
         // Warp gw owns rows 32*gw .. 32*gw+31 of the A tile; one instruction
         // copies 4 rows x 128 bytes (8 lanes per row, 16 bytes per lane) into
-        // the 128-byte-swizzled layout the UMMA descriptor expects.  Copies of
-        // a stage are completed, made visible to the tensor core's async
-        // proxy and announced on full[stage] with a lag of L stages, so L
-        // stages of copies stay in flight per thread.
-        constexpr int L = C::STAGES - 1;
+        // the 128-byte-swizzled layout the UMMA descriptor expects.  Each
+        // thread announces a stage on full[stage] with a non-incrementing
+        // cp.async arrive, so no thread waits for its own copies; the MMA
+        // thread makes them visible to the tensor core (proxy fence) after
+        // acquiring the barrier.
         const int gw = warp - 6;
         const int sub = lane >> 3, chunk = lane & 7;
         int stage = 0;
         uint32_t phase = 0;
-        int pending = 0;  // committed groups not yet announced (consecutive stages)
-        int last_stage = 0;
         for (int i = blockIdx.x; i < sch.n_total && !*s_abort; i += gridDim.x) {
             const Item it = decode_item(sch, i);
             if (it.zero) continue;
@@ -312,6 +306,9 @@ __global__ void __launch_bounds__(mn_threads(GATHER), 1)
             const int rows_valid = min(BM, sch.counts[it.g] - it.m * BM);
             const int my_row = 32 * gw + lane;
             const int my_tok = my_row < rows_valid ? ld_nc_s32(pg + it.m * BM + my_row) : -1;
+            int toks[8];
+#pragma unroll
+            for (int q = 0; q < 8; ++q) toks[q] = __shfl_sync(0xffffffffu, my_tok, 4 * q + sub);
             for (int kb = 0; kb < k_blocks; ++kb) {
                 int ok = 1;
                 if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, args.status);
@@ -320,29 +317,17 @@ __global__ void __launch_bounds__(mn_threads(GATHER), 1)
                 const uint32_t sa = smem_u32(stages + stage * C::STAGE_BYTES);
 #pragma unroll
                 for (int q = 0; q < 8; ++q) {
-                    const int rl = 4 * q + sub;  // row inside this warp's 32
-                    const int tok = __shfl_sync(0xffffffffu, my_tok, rl);
-                    const int row = 32 * gw + rl;
-                    if (tok >= 0) {
-                        const uint16_t *src = args.a_rows + static_cast<size_t>(tok) * args.K + kb * BK + chunk * 8;
+                    const int row = 32 * gw + 4 * q + sub;
+                    if (toks[q] >= 0) {
+                        const uint16_t *src = args.a_rows + static_cast<size_t>(toks[q]) * args.K + kb * BK + chunk * 8;
                         cp_async16(sa + row * 128 + ((chunk ^ (row & 7)) << 4), src);
                     }
                 }
-                cp_async_commit();
-                last_stage = stage;
-                if (++pending > L) {
-                    cp_async_wait<L>();
-                    fence_proxy_async_smem();
-                    mbar_arrive(&full[(stage + C::STAGES - L) % C::STAGES]);
-                    --pending;
-                }
+                cp_async_mbar_arrive_noinc(&full[stage]);
                 if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
             }
         }
-        cp_async_wait<0>();
-        fence_proxy_async_smem();
-        for (; pending > 0; --pending)
-            mbar_arrive(&full[(last_stage + C::STAGES - (pending - 1)) % C::STAGES]);
+        cp_async_wait_all();
     } else {
         // ===================== epilogue (warps 2..5) =====================
         const int quad = warp & 3;  // TMEM lanes 32*quad .. 32*quad+31
@@ -358,7 +343,7 @@ __global__ void __launch_bounds__(mn_threads(GATHER), 1)
             uint16_t *orow = args.out + static_cast<size_t>(token) * args.n_out + it.g * args.G;
             if (it.zero) {
                 if (valid)
-                    for (int cidx = 0; cidx < args.G; cidx += 8) st_global_v4(orow + cidx, 0, 0, 0, 0);
+                    for (int cidx = 0; cidx < args.G; cidx += 8) st_global_cs_v4(orow + cidx, 0, 0, 0, 0);
                 continue;
             }
             const bool active = j < sch.counts[it.g];
@@ -395,7 +380,7 @@ __global__ void __launch_bounds__(mn_threads(GATHER), 1)
                 if (valid) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
-                        st_global_v4(dst + cb + 8 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
+                        st_global_cs_v4(dst + cb + 8 * q, v[4 * q], v[4 * q + 1], v[4 * q + 2], v[4 * q + 3]);
                 }
             }
             tc_fence_before();
@@ -413,36 +398,28 @@ __global__ void __launch_bounds__(mn_threads(GATHER), 1)
     }
 }
 
-template <MNMode MODE, int BN_OP, Gather GATHER>
-cudaError_t launch_g(const CUtensorMap &tmA, const CUtensorMap &tmB0, const CUtensorMap &tmB1,
-                     const MNArgs &a, int num_sms, cudaStream_t s) {
+template <MNMode MODE, int BN_OP>
+cudaError_t launch_t(const CUtensorMap &tmB0, const CUtensorMap &tmB1, const MNArgs &a,
+                     int num_sms, cudaStream_t s) {
     using C = Cfg<MODE, BN_OP>;
-    auto kern = gemm_mn_kernel<MODE, BN_OP, GATHER>;
+    auto kern = gemm_mn_kernel<MODE, BN_OP>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
-    kern<<<num_sms, mn_threads(GATHER), C::SMEM_BYTES, s>>>(tmA, tmB0, tmB1, a);
+    kern<<<num_sms, kThreads, C::SMEM_BYTES, s>>>(tmB0, tmB1, a);
     return cudaGetLastError();
-}
-
-template <MNMode MODE, int BN_OP>
-cudaError_t launch_t(Gather g, const CUtensorMap &tmA, const CUtensorMap &tmB0,
-                     const CUtensorMap &tmB1, const MNArgs &a, int num_sms, cudaStream_t s) {
-    if (g == Gather::kCpAsync) return launch_g<MODE, BN_OP, Gather::kCpAsync>(tmA, tmB0, tmB1, a, num_sms, s);
-    return launch_g<MODE, BN_OP, Gather::kTma4>(tmA, tmB0, tmB1, a, num_sms, s);
 }
 
 }  // namespace
 
-cudaError_t launch_gemm_mn(MNMode mode, Gather g, int bn, const CUtensorMap &tmA,
-                           const CUtensorMap &tmB0, const CUtensorMap &tmB1, const MNArgs &a,
-                           int num_sms, cudaStream_t s) {
+cudaError_t launch_gemm_mn(MNMode mode, int bn, const CUtensorMap &tmB0, const CUtensorMap &tmB1,
+                           const MNArgs &a, int num_sms, cudaStream_t s) {
     if (mode == MNMode::kGateUp) {
-        if (bn == 128) return launch_t<MNMode::kGateUp, 128>(g, tmA, tmB0, tmB1, a, num_sms, s);
-        if (bn == 64) return launch_t<MNMode::kGateUp, 64>(g, tmA, tmB0, tmB1, a, num_sms, s);
+        if (bn == 128) return launch_t<MNMode::kGateUp, 128>(tmB0, tmB1, a, num_sms, s);
+        if (bn == 64) return launch_t<MNMode::kGateUp, 64>(tmB0, tmB1, a, num_sms, s);
     } else {
-        if (bn == 256) return launch_t<MNMode::kPlain, 256>(g, tmA, tmB0, tmB1, a, num_sms, s);
-        if (bn == 128) return launch_t<MNMode::kPlain, 128>(g, tmA, tmB0, tmB1, a, num_sms, s);
-        if (bn == 64) return launch_t<MNMode::kPlain, 64>(g, tmA, tmB0, tmB1, a, num_sms, s);
+        if (bn == 256) return launch_t<MNMode::kPlain, 256>(tmB0, tmB1, a, num_sms, s);
+        if (bn == 128) return launch_t<MNMode::kPlain, 128>(tmB0, tmB1, a, num_sms, s);
+        if (bn == 64) return launch_t<MNMode::kPlain, 64>(tmB0, tmB1, a, num_sms, s);
     }
     return cudaErrorInvalidValue;
 }

@@ -11,15 +11,13 @@ namespace wide {
 // GEMM-MN flavours: plain projection or fused silu(gate) * up.
 enum class MNMode { kPlain = 0, kGateUp = 1 };
 
-// How GEMM-MN brings the gathered token rows (operand A) into shared memory.
-enum class Gather { kTma4 = 0, kCpAsync = 1 };
-
 struct MNArgs {
-    const uint16_t *a_rows; // bf16 [T, K] token-row operand (for the cp.async gather)
+    const uint16_t *a_rows; // bf16 [T, K] token-row operand, gathered through perm
     const int32_t *perm;    // [n_groups, T]
     const int32_t *counts;  // [n_groups]
     uint16_t *out;          // bf16 [T, n_out]
     int T, K, n_out, G;
+    int bands;              // token bands of the tile order (bands * n_groups <= kMaxGroups)
     int *status;
 };
 
@@ -39,14 +37,15 @@ struct DecodeArgs {
     int T, K, N, G;
 };
 
+// Largest n_groups the GEMM kernels keep in shared memory.
+constexpr int kMaxGroups = 1024;
+
 cudaError_t launch_reorder(const uint8_t *mask, int T, int n_groups, int32_t *perm,
                            int32_t *counts, cudaStream_t s);
 
-// tmA: gather4 map over the token-row operand [T, K] (box 64 x 1, 128-B swizzle)
 // tmB0/tmB1: tiled maps over the weights [n_out, K] (box 64 x bn, 128-B swizzle)
-cudaError_t launch_gemm_mn(MNMode mode, Gather gather, int bn, const CUtensorMap &tmA, const CUtensorMap &tmB0,
-                           const CUtensorMap &tmB1, const MNArgs &a, int num_sms,
-                           cudaStream_t s);
+cudaError_t launch_gemm_mn(MNMode mode, int bn, const CUtensorMap &tmB0, const CUtensorMap &tmB1,
+                           const MNArgs &a, int num_sms, cudaStream_t s);
 
 // tmA: tiled map over the token-row operand [T, K] (box 64 x 128)
 // tmB: tiled map over the weights [N, K] (box 64 x bn)
@@ -55,8 +54,5 @@ cudaError_t launch_gemm_k(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB
 
 cudaError_t launch_decode_mn(MNMode mode, const DecodeArgs &a, int num_sms, cudaStream_t s);
 cudaError_t launch_decode_k(const DecodeArgs &a, int num_sms, cudaStream_t s);
-
-// Largest n_groups the GEMM kernels keep in shared memory.
-constexpr int kMaxGroups = 1024;
 
 }  // namespace wide
