@@ -4,6 +4,7 @@
 // word.  No call allocates, frees or synchronises (except wide_device_status).
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "../../include/wide.h"
@@ -13,6 +14,7 @@
 namespace wide {
 size_t decode_mn_smem_bytes(int T, int K, int n_groups);
 int gemm_k_max_groups();
+int gemm_k_pair_max_groups();
 }  // namespace wide
 
 namespace {
@@ -157,6 +159,15 @@ wide_status_t run_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask, i
     if (T <= kDecodeMaxT) {
         wide::DecodeArgs a{A, W, nullptr, mask, out, T, K, N, G};
         return from_cuda(wide::launch_decode_k(a, ctx.num_sms, s));
+    }
+    const char *pv = std::getenv("WIDE_K_PAIR");
+    const bool pair_ok = !(pv && pv[0] == '0');
+    if (pair_ok && N % 256 == 0 && K / G <= wide::gemm_k_pair_max_groups()) {
+        CUtensorMap tmA, tmB;
+        if ((st = encode_bf16_2d(&tmA, A, T, K, 128)) != WIDE_OK) return st;
+        if ((st = encode_bf16_2d(&tmB, W, N, K, 128)) != WIDE_OK) return st;
+        wide::KArgs a{mask, out, T, K, N, G, ctx.status};
+        return from_cuda(wide::launch_gemm_k_pair(tmA, tmB, a, ctx.num_sms, s));
     }
     const int bn = N % 256 == 0 ? 256 : N % 128 == 0 ? 128 : 64;
     CUtensorMap tmA, tmB;
