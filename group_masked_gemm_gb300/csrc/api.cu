@@ -4,7 +4,6 @@
 // word.  No call allocates, frees or synchronises (except wide_device_status).
 #include <cudaTypedefs.h>
 
-#include <cstdlib>
 #include <mutex>
 
 #include "../../include/wide.h"
@@ -12,9 +11,7 @@
 #include "internal.h"
 
 namespace wide {
-size_t decode_mn_smem_bytes(int T, int K, int n_groups);
 int gemm_k_max_groups();
-int gemm_k_pair_max_groups();
 }  // namespace wide
 
 namespace {
@@ -119,6 +116,7 @@ wide_status_t check_k(const void *A, const void *W, const void *mask, int T, int
     if (K / G > wide::gemm_k_max_groups()) return WIDE_ERR_UNSUPPORTED;
     const size_t need = wide_gemm_k_workspace_size(T, K, N, G);
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return WIDE_ERR_WORKSPACE;
+    if (need > 0 && !aligned16(ws)) return WIDE_ERR_INVALID_ARG;
     return WIDE_OK;
 }
 
@@ -151,23 +149,14 @@ wide_status_t run_mn(wide::MNMode mode, const uint16_t *X, const uint16_t *W0,
 }
 
 wide_status_t run_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask, int T, int K,
-                    int N, int G, uint16_t *out, void *stream) {
+                    int N, int G, uint16_t *out, void *ws, void *stream) {
     DeviceCtx ctx;
     wide_status_t st = device_ctx(&ctx);
     if (st != WIDE_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     if (T <= kDecodeMaxT) {
         wide::DecodeArgs a{A, W, nullptr, mask, out, T, K, N, G};
-        return from_cuda(wide::launch_decode_k(a, ctx.num_sms, s));
-    }
-    const char *pv = std::getenv("WIDE_K_PAIR");
-    const bool pair_ok = !(pv && pv[0] == '0');
-    if (pair_ok && N % 256 == 0 && K / G <= wide::gemm_k_pair_max_groups()) {
-        CUtensorMap tmA, tmB;
-        if ((st = encode_bf16_2d(&tmA, A, T, K, 128)) != WIDE_OK) return st;
-        if ((st = encode_bf16_2d(&tmB, W, N, K, 128)) != WIDE_OK) return st;
-        wide::KArgs a{mask, out, T, K, N, G, ctx.status};
-        return from_cuda(wide::launch_gemm_k_pair(tmA, tmB, a, ctx.num_sms, s));
+        return from_cuda(wide::launch_decode_k(a, static_cast<float *>(ws), s));
     }
     const int bn = N % 256 == 0 ? 256 : N % 128 == 0 ? 128 : 64;
     CUtensorMap tmA, tmB;
@@ -236,11 +225,10 @@ wide_status_t wide_proj_mn(const uint16_t *X, const uint16_t *W, const uint8_t *
 }
 
 size_t wide_gemm_k_workspace_size(int T, int K, int N, int G) {
-    (void)T;
-    (void)K;
-    (void)N;
-    (void)G;
-    return 0;
+    // Prefill (T > 16) reduces in TMEM and needs none; the decode path sums
+    // fp32 partials of the split reduction dimension.
+    if (T < 1 || T > kDecodeMaxT || G <= 0 || K < G || K % G) return 0;
+    return wide::decode_k_workspace_bytes(T, K, N, G);
 }
 
 wide_status_t wide_gemm_k_down(const uint16_t *H, const uint16_t *W_down, const uint8_t *mask,
@@ -251,7 +239,7 @@ wide_status_t wide_gemm_k_down(const uint16_t *H, const uint16_t *W_down, const 
     (void)counts;
     wide_status_t st = check_k(H, W_down, mask, T, d_ffn, d_model, G, Y, ws, ws_bytes);
     if (st != WIDE_OK) return st;
-    return run_k(H, W_down, mask, T, d_ffn, d_model, G, Y, stream);
+    return run_k(H, W_down, mask, T, d_ffn, d_model, G, Y, ws, stream);
 }
 
 wide_status_t wide_proj_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask,
@@ -261,7 +249,7 @@ wide_status_t wide_proj_k(const uint16_t *A, const uint16_t *W, const uint8_t *m
     (void)counts;
     wide_status_t st = check_k(A, W, mask, T, K, N, G, Y, ws, ws_bytes);
     if (st != WIDE_OK) return st;
-    return run_k(A, W, mask, T, K, N, G, Y, stream);
+    return run_k(A, W, mask, T, K, N, G, Y, ws, stream);
 }
 
 wide_status_t wide_device_status(void *stream) {

@@ -3,15 +3,18 @@
 // bypassed and routing is checked directly at block level).
 //
 // With at most 16 tokens the work is bound by HBM reads of the weights, so
-// the kernels stream only the weight groups that at least one token uses
-// (the union of the tokens' active groups) with 16-byte non-allocating loads
-// and keep the few token rows on chip.
-//   decode_mn: one warp per output feature n (gate and up rows together),
-//              X staged once per persistent CTA in shared memory.
-//   decode_k : a CTA owns 16 output features; the reduction dimension is
-//              walked in chunks whose token rows are staged, already masked
-//              (inactive groups zeroed), in shared memory; loads of W[n, K_g]
-//              are issued only for groups in the token union.
+// the kernels read only the weight groups that at least one token uses (the
+// union of the tokens' active groups), with 16-byte non-allocating loads
+// issued a whole chunk at a time (8 x 512 B per warp and weight row) so that
+// enough bytes are in flight to cover the HBM latency.
+//   decode_mn:  one warp per output feature n (gate and up rows together),
+//               X staged once per persistent CTA in shared memory.
+//   decode_k :  the reduction dimension is split, on group boundaries, over
+//               gridDim.y CTAs; each CTA stages its slice of the token rows
+//               (inactive groups zeroed) once, streams 16 output rows of W
+//               and writes fp32 partial sums to the workspace; a second
+//               kernel adds the partials of each output in split order
+//               (deterministic) and rounds to bf16.
 #include "common.cuh"
 #include "internal.h"
 
@@ -20,6 +23,8 @@ namespace {
 
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
+constexpr int kChunkIters = 8;      // 256-element steps whose loads are issued together
+constexpr int kSliceBytes = 96 * 1024;  // staged token-row slice of one decode_k CTA
 
 __device__ __forceinline__ uint4 ld_stream16(const void *p) {
     uint4 v;
@@ -49,13 +54,13 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
     return *reinterpret_cast<uint16_t *>(&h);
 }
 
-// Per-group bitmask of active tokens (bit t set when M[t, g] != 0).
-__device__ __forceinline__ void build_group_bits(const uint8_t *mask, int T, int ng,
-                                                 uint32_t *gbits) {
-    for (int g = threadIdx.x; g < ng; g += blockDim.x) {
+// Per-group bitmask of active tokens (bit t set when M[t, g] != 0), groups [g0, g1).
+__device__ __forceinline__ void build_group_bits(const uint8_t *mask, int T, int ng, int g0,
+                                                 int g1, uint32_t *gbits) {
+    for (int g = g0 + static_cast<int>(threadIdx.x); g < g1; g += blockDim.x) {
         uint32_t b = 0;
         for (int t = 0; t < T; ++t) b |= static_cast<uint32_t>(mask[t * ng + g] != 0) << t;
-        gbits[g] = b;
+        gbits[g - g0] = b;
     }
 }
 
@@ -70,7 +75,7 @@ __global__ void __launch_bounds__(kThreads)
 
     for (int v = threadIdx.x; v < T * K / 8; v += kThreads)
         reinterpret_cast<uint4 *>(xs)[v] = reinterpret_cast<const uint4 *>(a.x)[v];
-    build_group_bits(a.mask, T, ng, gbits);
+    build_group_bits(a.mask, T, ng, 0, ng, gbits);
     __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -86,20 +91,33 @@ __global__ void __launch_bounds__(kThreads)
         for (int t = 0; t < TM; ++t) acc0[t] = acc1[t] = 0.f;
         const uint16_t *w0 = a.w0 + static_cast<size_t>(n) * K;
         const uint16_t *w1 = MODE == MNMode::kGateUp ? a.w1 + static_cast<size_t>(n) * K : nullptr;
-#pragma unroll 4
-        for (int k = lane * 8; k < K; k += 256) {
-            float f0[8], f1[8];
-            bf16x8_to_f32(ld_stream16(w0 + k), f0);
-            if (MODE == MNMode::kGateUp) bf16x8_to_f32(ld_stream16(w1 + k), f1);
+        for (int kc = 0; kc < K; kc += 256 * kChunkIters) {
+            uint4 r0[kChunkIters], r1[kChunkIters];
 #pragma unroll
-            for (int t = 0; t < TM; ++t) {
-                if (t < T && ((bits >> t) & 1u)) {
-                    float xf[8];
-                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xs + t * K + k), xf);
+            for (int j = 0; j < kChunkIters; ++j) {
+                const int k = kc + 256 * j + lane * 8;
+                if (k < K) {
+                    r0[j] = ld_stream16(w0 + k);
+                    if (MODE == MNMode::kGateUp) r1[j] = ld_stream16(w1 + k);
+                }
+            }
 #pragma unroll
-                    for (int e = 0; e < 8; ++e) {
-                        acc0[t] = fmaf(f0[e], xf[e], acc0[t]);
-                        if (MODE == MNMode::kGateUp) acc1[t] = fmaf(f1[e], xf[e], acc1[t]);
+            for (int j = 0; j < kChunkIters; ++j) {
+                const int k = kc + 256 * j + lane * 8;
+                if (k >= K) break;
+                float f0[8], f1[8];
+                bf16x8_to_f32(r0[j], f0);
+                if (MODE == MNMode::kGateUp) bf16x8_to_f32(r1[j], f1);
+#pragma unroll
+                for (int t = 0; t < TM; ++t) {
+                    if (t < T && ((bits >> t) & 1u)) {
+                        float xf[8];
+                        bf16x8_to_f32(*reinterpret_cast<const uint4 *>(xs + t * K + k), xf);
+#pragma unroll
+                        for (int e = 0; e < 8; ++e) {
+                            acc0[t] = fmaf(f0[e], xf[e], acc0[t]);
+                            if (MODE == MNMode::kGateUp) acc1[t] = fmaf(f1[e], xf[e], acc1[t]);
+                        }
                     }
                 }
             }
@@ -121,17 +139,34 @@ __global__ void __launch_bounds__(kThreads)
 
 constexpr int kRowsPerWarp = 2;
 constexpr int kRowsPerCta = kWarps * kRowsPerWarp;
-constexpr int kChunk = 1024;  // reduction columns staged per step
 
+// Partial sums of one split (blockIdx.y) of the reduction dimension for 16
+// output rows: ws[split][t][n] (fp32).
 template <int TM>
 __global__ void __launch_bounds__(kThreads)
-    decode_k_kernel(const DecodeArgs a) {
-    __shared__ __align__(16) uint16_t as[TM * kChunk];
-    extern __shared__ __align__(16) uint8_t dsmem[];
-    uint32_t *gbits = reinterpret_cast<uint32_t *>(dsmem);
+    decode_k_partial_kernel(const DecodeArgs a, int groups_per_split, float *ws) {
+    extern __shared__ __align__(16) uint8_t smem[];
     const int T = a.T, K = a.K, N = a.N, G = a.G;
     const int ng = K / G;
-    build_group_bits(a.mask, T, ng, gbits);
+    const int g_begin = blockIdx.y * groups_per_split;
+    const int g_end = min(ng, g_begin + groups_per_split);
+    const int k0 = g_begin * G;
+    const int klen = (g_end - g_begin) * G;
+    const int kstride = groups_per_split * G;  // row stride of the staged slice
+    uint16_t *as = reinterpret_cast<uint16_t *>(smem);                                  // [TM][kstride]
+    uint32_t *gbits = reinterpret_cast<uint32_t *>(smem + static_cast<size_t>(TM) * kstride * 2);
+
+    build_group_bits(a.mask, T, ng, g_begin, g_end, gbits);
+    __syncthreads();
+    const int vec_per_row = klen / 8;
+    for (int v = threadIdx.x; v < T * vec_per_row; v += kThreads) {
+        const int t = v / vec_per_row, k = (v - t * vec_per_row) * 8;
+        uint4 val = make_uint4(0, 0, 0, 0);
+        if ((gbits[k / G] >> t) & 1u)
+            val = *reinterpret_cast<const uint4 *>(a.x + static_cast<size_t>(t) * K + k0 + k);
+        *reinterpret_cast<uint4 *>(as + t * kstride + k) = val;
+    }
+    __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n0 = blockIdx.x * kRowsPerCta + warp * kRowsPerWarp;
@@ -141,30 +176,32 @@ __global__ void __launch_bounds__(kThreads)
 #pragma unroll
         for (int t = 0; t < TM; ++t) acc[r][t] = 0.f;
 
-    for (int kc = 0; kc < K; kc += kChunk) {
-        const int len = min(kChunk, K - kc);
-        __syncthreads();  // previous chunk consumed; gbits ready on the first pass
-        for (int v = threadIdx.x; v < T * (len / 8); v += kThreads) {
-            const int t = v / (len / 8), k = (v - t * (len / 8)) * 8;
-            const bool on = (gbits[(kc + k) / G] >> t) & 1u;
-            uint4 val = make_uint4(0, 0, 0, 0);
-            if (on) val = *reinterpret_cast<const uint4 *>(a.x + static_cast<size_t>(t) * K + kc + k);
-            *reinterpret_cast<uint4 *>(as + t * kChunk + k) = val;
+    for (int kc = 0; kc < klen; kc += 256 * kChunkIters) {
+        uint4 wr[kChunkIters][kRowsPerWarp];
+#pragma unroll
+        for (int j = 0; j < kChunkIters; ++j) {
+            const int k = kc + 256 * j + lane * 8;
+            // a group no token uses is never read
+            if (k < klen && gbits[k / G] != 0u) {
+#pragma unroll
+                for (int r = 0; r < kRowsPerWarp; ++r)
+                    wr[j][r] = ld_stream16(a.w0 + static_cast<size_t>(n0 + r) * K + k0 + k);
+            }
         }
-        __syncthreads();
-#pragma unroll 2
-        for (int k = lane * 8; k < len; k += 256) {
-            const uint32_t bits = gbits[(kc + k) / G];
-            if (bits == 0) continue;  // no token uses this group: its weights are never read
+#pragma unroll
+        for (int j = 0; j < kChunkIters; ++j) {
+            const int k = kc + 256 * j + lane * 8;
+            if (k >= klen) break;
+            const uint32_t bits = gbits[k / G];
+            if (bits == 0u) continue;
             float w[kRowsPerWarp][8];
 #pragma unroll
-            for (int r = 0; r < kRowsPerWarp; ++r)
-                bf16x8_to_f32(ld_stream16(a.w0 + static_cast<size_t>(n0 + r) * K + kc + k), w[r]);
+            for (int r = 0; r < kRowsPerWarp; ++r) bf16x8_to_f32(wr[j][r], w[r]);
 #pragma unroll
             for (int t = 0; t < TM; ++t) {
                 if (t < T && ((bits >> t) & 1u)) {
                     float xf[8];
-                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(as + t * kChunk + k), xf);
+                    bf16x8_to_f32(*reinterpret_cast<const uint4 *>(as + t * kstride + k), xf);
 #pragma unroll
                     for (int r = 0; r < kRowsPerWarp; ++r)
 #pragma unroll
@@ -173,14 +210,25 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
     }
+    float *out = ws + static_cast<size_t>(blockIdx.y) * T * N;
 #pragma unroll
     for (int r = 0; r < kRowsPerWarp; ++r)
 #pragma unroll
         for (int t = 0; t < TM; ++t) {
             if (t >= T) break;
             const float s = warp_sum(acc[r][t]);
-            if (lane == 0) a.out[static_cast<size_t>(t) * N + n0 + r] = f32_to_bf16_bits(s);
+            if (lane == 0) out[static_cast<size_t>(t) * N + n0 + r] = s;
         }
+}
+
+// Y[t][n] = bf16( sum over splits s = 0, 1, ... of ws[s][t][n] ).
+__global__ void __launch_bounds__(kThreads)
+    decode_k_finalize_kernel(const float *ws, int splits, int TN, uint16_t *out) {
+    const int i = blockIdx.x * kThreads + threadIdx.x;
+    if (i >= TN) return;
+    float s = 0.f;
+    for (int p = 0; p < splits; ++p) s += ws[static_cast<size_t>(p) * TN + i];
+    out[i] = f32_to_bf16_bits(s);
 }
 
 template <MNMode MODE, int TM>
@@ -191,23 +239,35 @@ cudaError_t launch_mn_t(const DecodeArgs &a, int num_sms, cudaStream_t s) {
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int rows_blocks = (a.N + kWarps - 1) / kWarps;
-    const int grid = rows_blocks < 2 * num_sms ? rows_blocks : 2 * num_sms;
+    const int per_sm = smem <= 100 * 1024 ? 2 : 1;
+    const int grid = rows_blocks < per_sm * num_sms ? rows_blocks : per_sm * num_sms;
     kern<<<grid, kThreads, smem, s>>>(a);
     return cudaGetLastError();
 }
 
-template <int TM>
-cudaError_t launch_k_t(const DecodeArgs &a, cudaStream_t s) {
-    const size_t smem = static_cast<size_t>(a.K / a.G) * 4;
-    decode_k_kernel<TM><<<a.N / kRowsPerCta, kThreads, smem, s>>>(a);
-    return cudaGetLastError();
-}
+int tm_of(int T) { return T <= 1 ? 1 : T <= 4 ? 4 : 16; }
 
 }  // namespace
 
 size_t decode_mn_smem_bytes(int T, int K, int n_groups) {
-    const int tm = T <= 1 ? 1 : T <= 4 ? 4 : 16;
-    return static_cast<size_t>(tm) * K * 2 + static_cast<size_t>(n_groups) * 4;
+    return static_cast<size_t>(tm_of(T)) * K * 2 + static_cast<size_t>(n_groups) * 4;
+}
+
+// Groups per split of the reduction dimension: the staged slice of TM token
+// rows fits kSliceBytes.
+int decode_k_groups_per_split(int T, int K, int G) {
+    const int ng = K / G;
+    int gps_max = kSliceBytes / (tm_of(T) * G * 2);
+    if (gps_max < 1) gps_max = 1;
+    const int splits = (ng + gps_max - 1) / gps_max;
+    return (ng + splits - 1) / splits;  // equal splits on group boundaries
+}
+
+size_t decode_k_workspace_bytes(int T, int K, int N, int G) {
+    const int ng = K / G;
+    const int gps = decode_k_groups_per_split(T, K, G);
+    const int splits = (ng + gps - 1) / gps;
+    return static_cast<size_t>(splits) * T * N * sizeof(float);
 }
 
 cudaError_t launch_decode_mn(MNMode mode, const DecodeArgs &a, int num_sms, cudaStream_t s) {
@@ -221,11 +281,30 @@ cudaError_t launch_decode_mn(MNMode mode, const DecodeArgs &a, int num_sms, cuda
     return launch_mn_t<MNMode::kPlain, 16>(a, num_sms, s);
 }
 
-cudaError_t launch_decode_k(const DecodeArgs &a, int num_sms, cudaStream_t s) {
-    (void)num_sms;
-    if (a.T <= 1) return launch_k_t<1>(a, s);
-    if (a.T <= 4) return launch_k_t<4>(a, s);
-    return launch_k_t<16>(a, s);
+template <int TM>
+static cudaError_t launch_k_partial(const DecodeArgs &a, int gps, int splits, float *ws,
+                                    cudaStream_t s) {
+    auto kern = decode_k_partial_kernel<TM>;
+    const size_t smem = static_cast<size_t>(TM) * gps * a.G * 2 + static_cast<size_t>(gps) * 4;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    kern<<<dim3(a.N / kRowsPerCta, splits), kThreads, smem, s>>>(a, gps, ws);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_decode_k(const DecodeArgs &a, float *ws, cudaStream_t s) {
+    const int ng = a.K / a.G;
+    const int gps = decode_k_groups_per_split(a.T, a.K, a.G);
+    const int splits = (ng + gps - 1) / gps;
+    cudaError_t e;
+    if (a.T <= 1) e = launch_k_partial<1>(a, gps, splits, ws, s);
+    else if (a.T <= 4) e = launch_k_partial<4>(a, gps, splits, ws, s);
+    else e = launch_k_partial<16>(a, gps, splits, ws, s);
+    if (e != cudaSuccess) return e;
+    const int TN = a.T * a.N;
+    decode_k_finalize_kernel<<<(TN + kThreads - 1) / kThreads, kThreads, 0, s>>>(ws, splits, TN, a.out);
+    return cudaGetLastError();
 }
 
 }  // namespace wide

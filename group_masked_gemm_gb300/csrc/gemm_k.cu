@@ -63,6 +63,75 @@ __device__ __forceinline__ MaskBuf mask_buf(uint8_t *area, int b) {
                    reinterpret_cast<int *>(base + kMaxKGroups * 20)};
 }
 
+
+// Lane masks and live-group list of one tile of Q*32 tokens starting at m0:
+// for every group g, word q (q < Q) has bit i set when token m0+32q+i is
+// INACTIVE (or beyond T); the group is live when any token is active.  Runs
+// on one warp.  When n_groups is a multiple of 16 each lane reads 16 groups
+// of a token row with one 16-byte load.
+template <int Q>
+__device__ __forceinline__ int build_tile_masks(const uint8_t *__restrict__ mask, int T, int ng,
+                                                int m0, uint32_t *lanes, int *live) {
+    const int lane = threadIdx.x & 31;
+    int n_live = 0;
+    auto emit = [&](int g, const uint32_t (&w)[Q]) {
+        uint32_t mine = 0, any = 0;
+#pragma unroll
+        for (int q = 0; q < Q; ++q) {
+            any |= w[q];
+            if (lane == q) mine = w[q];
+        }
+        if (lane < Q) lanes[g * Q + lane] = ~mine;
+        if (any != 0u) {
+            if (lane == 0) live[n_live] = g;
+            ++n_live;
+        }
+    };
+    if ((ng & 15) == 0) {
+        for (int g0 = 0; g0 < ng; g0 += 16) {
+            uint4 v[Q];
+#pragma unroll
+            for (int q = 0; q < Q; ++q) {
+                const int t = m0 + 32 * q + lane;
+                v[q] = t < T ? *reinterpret_cast<const uint4 *>(mask + static_cast<size_t>(t) * ng + g0)
+                             : make_uint4(0, 0, 0, 0);
+            }
+#pragma unroll
+            for (int u = 0; u < 16; ++u) {
+                uint32_t w[Q];
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {
+                    const uint32_t word = u < 4 ? v[q].x : u < 8 ? v[q].y : u < 12 ? v[q].z : v[q].w;
+                    w[q] = __ballot_sync(0xffffffffu, ((word >> ((u & 3) * 8)) & 0xFFu) != 0u);
+                }
+                emit(g0 + u, w);
+            }
+        }
+    } else {
+        constexpr int kU = 4;
+        for (int g0 = 0; g0 < ng; g0 += kU) {
+            uint8_t v[kU][Q];
+#pragma unroll
+            for (int u = 0; u < kU; ++u)
+#pragma unroll
+                for (int q = 0; q < Q; ++q) {
+                    const int t = m0 + 32 * q + lane;
+                    const int g = g0 + u;
+                    v[u][q] = (t < T && g < ng) ? mask[static_cast<size_t>(t) * ng + g] : 0;
+                }
+#pragma unroll
+            for (int u = 0; u < kU; ++u) {
+                if (g0 + u >= ng) break;
+                uint32_t w[Q];
+#pragma unroll
+                for (int q = 0; q < Q; ++q) w[q] = __ballot_sync(0xffffffffu, v[u][q] != 0);
+                emit(g0 + u, w);
+            }
+        }
+    }
+    return n_live;
+}
+
 template <int BN>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_k_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -146,36 +215,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { *s_abort = 1; break; }
             const MaskBuf mbuf = mask_buf<C::MASK_BUF_BYTES>(mask_area, b);
-            int n_live = 0;
-            constexpr int kU = 8;  // groups per batch of independent loads
-            for (int g0 = 0; g0 < ng; g0 += kU) {
-                uint8_t v[kU][4];
-#pragma unroll
-                for (int u = 0; u < kU; ++u)
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) {
-                        const int t = m0 + 32 * q + lane;
-                        const int g = g0 + u;
-                        v[u][q] = (t < T && g < ng) ? args.mask[static_cast<size_t>(t) * ng + g] : 0;
-                    }
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int g = g0 + u;
-                    if (g >= ng) break;
-                    uint32_t w[4];
-#pragma unroll
-                    for (int q = 0; q < 4; ++q) w[q] = __ballot_sync(0xffffffffu, v[u][q] != 0);
-                    const bool live = (w[0] | w[1] | w[2] | w[3]) != 0u;
-                    if (lane < 4) {
-                        const uint32_t wl = lane == 0 ? w[0] : lane == 1 ? w[1] : lane == 2 ? w[2] : w[3];
-                        mbuf.lanes[g * 4 + lane] = ~wl;
-                    }
-                    if (live) {
-                        if (lane == 0) mbuf.live[n_live] = g;
-                        ++n_live;
-                    }
-                }
-            }
+            const int n_live = build_tile_masks<4>(args.mask, T, ng, m0, mbuf.lanes, mbuf.live);
             if (lane == 0) *mbuf.n_live = n_live;
             __threadfence_block();
             __syncwarp();
@@ -336,341 +376,10 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs
 }
 
 
-// ---------------------------------------------------------------------------
-// CTA-pair variant (cluster of 2, tcgen05 cta_group::2): the pair owns 256
-// tokens x BN columns.  Each CTA loads its own 128 token rows and half of the
-// BN weight rows into its shared memory; the even CTA issues M = 256 MMAs
-// that read both CTAs' operands and write each CTA's 128 accumulator lanes.
-// Per SM this halves the weight bytes staged per MMA (32 KB instead of 48 KB
-// per 64-deep step).  Lane masks cover the pair's 256 tokens (8 words).
-constexpr int kMaxPairGroups = 256;
-
-template <int BN>
-struct KPairCfg {
-    static constexpr int BNH = BN / 2;  // weight rows loaded by each CTA
-    static constexpr int A_BYTES = BM * BK * 2;
-    static constexpr int B_BYTES = BNH * BK * 2;
-    static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
-    static constexpr int MASK_BUF_BYTES = kMaxPairGroups * 32 + kMaxPairGroups * 4 + 16;
-    static constexpr int BAR_BYTES = 256;
-    static constexpr int STAGES_FIT =
-        (kSmemBudget - 1024 - 2 * MASK_BUF_BYTES - BAR_BYTES) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
-    static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
-    static constexpr uint32_t IDESC = idesc_bf16_f32(2 * BM, BN);
-    static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * MASK_BUF_BYTES + BAR_BYTES;
-    static_assert(STAGES >= 2, "pipeline needs two stages");
-    static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
-};
-
-struct PairMaskBuf {
-    uint32_t *lanes;  // [ng][8] disable-output-lane words (even CTA's 4, then odd CTA's 4)
-    int *live;        // [ng]
-    int *n_live;
-};
-
-template <int BUF_BYTES>
-__device__ __forceinline__ PairMaskBuf pair_mask_buf(uint8_t *area, int b) {
-    uint8_t *base = area + b * BUF_BYTES;
-    return PairMaskBuf{reinterpret_cast<uint32_t *>(base),
-                       reinterpret_cast<int *>(base + kMaxPairGroups * 32),
-                       reinterpret_cast<int *>(base + kMaxPairGroups * 36)};
-}
-
-template <int BN>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
-    gemm_k_pair_kernel(const __grid_constant__ CUtensorMap tmA,
-                       const __grid_constant__ CUtensorMap tmB, const KArgs args) {
-    using C = KPairCfg<BN>;
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *stages = smem;
-    uint8_t *mask_area = smem + C::STAGES * C::STAGE_BYTES;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(mask_area + 2 * C::MASK_BUF_BYTES);
-    uint64_t *full = bars;                  // used in the even CTA: both CTAs' copies land here
-    uint64_t *empty = bars + C::STAGES;     // per CTA, released by the pair MMA commit
-    uint64_t *tfull = bars + 2 * C::STAGES; // per CTA
-    uint64_t *tempty = tfull + 2;           // even CTA: 4 epilogue warps x 2 CTAs
-    uint64_t *mfull = tempty + 2;
-    uint64_t *mempty = mfull + 2;
-    uint64_t *final_bar = mempty + 2;
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(final_bar + 1);
-    volatile int *s_abort = reinterpret_cast<volatile int *>(s_tmem + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t rank = cluster_ctarank();
-    const bool even = rank == 0;
-    const int T = args.T;
-    const int ng = args.K / args.G;
-    const int m_tiles = (T + 2 * BM - 1) / (2 * BM);
-    const int n_tiles = args.N / BN;
-    const int n_items = m_tiles * n_tiles;
-    const int kb_per_group = args.G / BK;
-    const int pair = blockIdx.x >> 1, n_pairs = gridDim.x >> 1;
-
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < C::STAGES; ++s) {
-            mbar_init(&full[s], 2);
-            mbar_init(&empty[s], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], 8);
-            mbar_init(&mfull[b], 1);
-            mbar_init(&mempty[b], 2);
-        }
-        mbar_init(final_bar, 1);
-        *s_abort = 0;
-        fence_barrier_init();
-    }
-    if (warp == 0 && lane == 0) {
-        prefetch_tmap(&tmA);
-        prefetch_tmap(&tmB);
-    }
-    if (warp == 1) {
-        tmem_alloc_pair(s_tmem, C::TMEM_COLS);
-        tmem_relinquish_pair();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *s_tmem;
-    if (warp >= 3) {
-        const int quad = warp & 3;
-        uint32_t z[32];
-#pragma unroll
-        for (int q = 0; q < 32; ++q) z[q] = 0u;
-        for (int col = 0; col < 2 * BN; col += 32)
-            tmem_st32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + col, z);
-        tmem_st_wait();
-    }
-    tc_fence_before();
-    cluster_sync();  // both CTAs' barriers initialised and accumulators zeroed
-    tc_fence_after();
-    const uint32_t full_even = mapa_shared(smem_u32(&full[0]), 0);
-    const uint32_t tempty_even = mapa_shared(smem_u32(&tempty[0]), 0);
-
-    if (warp == 2) {
-        // ===================== mask builder (both CTAs, the pair's 256 tokens) ====
-        int b = 0;
-        uint32_t bphase = 0;
-        for (int i = pair; i < n_items && !*s_abort; i += n_pairs) {
-            const int m0 = (i / n_tiles) * 2 * BM;
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait(&mempty[b], bphase ^ 1u, args.status);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) { *s_abort = 1; break; }
-            const PairMaskBuf mbuf = pair_mask_buf<C::MASK_BUF_BYTES>(mask_area, b);
-            int n_live = 0;
-            constexpr int kU = 4;
-            for (int g0 = 0; g0 < ng; g0 += kU) {
-                uint8_t v[kU][8];
-#pragma unroll
-                for (int u = 0; u < kU; ++u)
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const int t = m0 + 32 * q + lane;
-                        const int g = g0 + u;
-                        v[u][q] = (t < T && g < ng) ? args.mask[static_cast<size_t>(t) * ng + g] : 0;
-                    }
-#pragma unroll
-                for (int u = 0; u < kU; ++u) {
-                    const int g = g0 + u;
-                    if (g >= ng) break;
-                    uint32_t mine = 0, any = 0;
-#pragma unroll
-                    for (int q = 0; q < 8; ++q) {
-                        const uint32_t w = __ballot_sync(0xffffffffu, v[u][q] != 0);
-                        any |= w;
-                        if (lane == q) mine = w;
-                    }
-                    if (lane < 8) mbuf.lanes[g * 8 + lane] = ~mine;
-                    if (any != 0u) {
-                        if (lane == 0) mbuf.live[n_live] = g;
-                        ++n_live;
-                    }
-                }
-            }
-            if (lane == 0) *mbuf.n_live = n_live;
-            __threadfence_block();
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&mfull[b]);
-            if (++b == 2) { b = 0; bphase ^= 1u; }
-        }
-    } else if (warp == 0) {
-        // ===================== TMA producer (both CTAs) =====================
-        int stage = 0;
-        uint32_t phase = 0;
-        uint32_t used = 0, last_parity = 0;
-        int b = 0;
-        uint32_t bphase = 0;
-        for (int i = pair; i < n_items && !*s_abort; i += n_pairs) {
-            const int mt = i / n_tiles, nt = i - mt * n_tiles;
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait(&mfull[b], bphase, args.status);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) { *s_abort = 1; break; }
-            const PairMaskBuf mbuf = pair_mask_buf<C::MASK_BUF_BYTES>(mask_area, b);
-            const int n_live = *mbuf.n_live;
-            const int row_a = mt * 2 * BM + static_cast<int>(rank) * BM;
-            const int row_b = nt * BN + static_cast<int>(rank) * C::BNH;
-            for (int li = 0; li < n_live && ok; ++li) {
-                const int g = mbuf.live[li];
-                for (int kb = 0; kb < kb_per_group; ++kb) {
-                    if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, args.status);
-                    ok = __shfl_sync(0xffffffffu, ok, 0);
-                    if (!ok) break;
-                    if (lane == 0) {
-                        const uint32_t sa = smem_u32(stages + stage * C::STAGE_BYTES);
-                        const uint32_t bar = full_even + 8u * stage;
-                        mbar_arrive_expect_tx_cluster(bar, C::STAGE_BYTES);
-                        const int kx = g * args.G + kb * BK;
-                        tma_load_2d_pair(sa, &tmA, bar, kx, row_a);
-                        tma_load_2d_pair(sa + C::A_BYTES, &tmB, bar, kx, row_b);
-                    }
-                    used |= 1u << stage;
-                    last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-                    if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
-                }
-            }
-            if (!ok) { *s_abort = 1; break; }
-            __syncwarp();
-            if (lane == 0) mbar_arrive(&mempty[b]);
-            if (++b == 2) { b = 0; bphase ^= 1u; }
-        }
-        // the even CTA's full barriers count both CTAs' bytes: once they have
-        // all completed, no copy of the pair is still landing
-        if (even && lane == 0)
-            for (int s = 0; s < C::STAGES; ++s)
-                if (used & (1u << s)) mbar_wait(&full[s], (last_parity >> s) & 1u, args.status);
-        __syncwarp();
-    } else if (warp == 1) {
-        // ===================== pair MMA issuer (even CTA) =====================
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            int acc = 0;
-            uint32_t acc_phase = 0;
-            int b = 0;
-            uint32_t bphase = 0;
-            for (int i = pair; i < n_items && !*s_abort; i += n_pairs) {
-                if (!mbar_wait(&mfull[b], bphase, args.status)) { *s_abort = 1; break; }
-                if (even) {
-                    if (!mbar_wait(&tempty[acc], acc_phase ^ 1u, args.status)) { *s_abort = 1; break; }
-                    tc_fence_after();
-                    const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
-                    const PairMaskBuf mbuf = pair_mask_buf<C::MASK_BUF_BYTES>(mask_area, b);
-                    const int n_live = *mbuf.n_live;
-                    bool ok = true;
-                    for (int li = 0; li < n_live && ok; ++li) {
-                        const int g = mbuf.live[li];
-                        uint32_t lm[8];
-#pragma unroll
-                        for (int q = 0; q < 8; ++q) lm[q] = mbuf.lanes[g * 8 + q];
-                        for (int kb = 0; kb < kb_per_group; ++kb) {
-                            if (!mbar_wait(&full[stage], phase, args.status)) { ok = false; break; }
-                            tc_fence_after();
-                            const uint32_t a0 = smem_u32(stages + stage * C::STAGE_BYTES);
-                            const uint32_t b0 = a0 + C::A_BYTES;
-#pragma unroll
-                            for (int kk = 0; kk < BK / 16; ++kk)
-                                mma_bf16_pair_lanemask(d, sw128_kmajor_desc(a0 + kk * 32),
-                                                       sw128_kmajor_desc(b0 + kk * 32), C::IDESC, lm);
-                            mma_commit_pair(&empty[stage], 0x3);
-                            if (++stage == C::STAGES) { stage = 0; phase ^= 1u; }
-                        }
-                    }
-                    if (!ok) { *s_abort = 1; break; }
-                    mma_commit_pair(&tfull[acc], 0x3);
-                    if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
-                }
-                mbar_arrive(&mempty[b]);
-                if (++b == 2) { b = 0; bphase ^= 1u; }
-            }
-            if (even) {
-                mma_commit_pair(final_bar, 0x1);
-                mbar_wait(final_bar, 0, args.status);
-            }
-        }
-        __syncwarp();
-    } else {
-        // ===================== epilogue (warps 3..6, both CTAs) =====================
-        const int quad = warp & 3;
-        const int row = quad * 32 + lane;
-        int acc = 0;
-        uint32_t acc_phase = 0;
-        uint32_t z[32];
-#pragma unroll
-        for (int q = 0; q < 32; ++q) z[q] = 0u;
-        for (int i = pair; i < n_items && !*s_abort; i += n_pairs) {
-            const int mt = i / n_tiles, nt = i - mt * n_tiles;
-            const int t = mt * 2 * BM + static_cast<int>(rank) * BM + row;
-            int ok = 1;
-            if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, args.status);
-            ok = __shfl_sync(0xffffffffu, ok, 0);
-            if (!ok) { *s_abort = 1; break; }
-            tc_fence_after();
-            const uint32_t taddr = tmem_base + (static_cast<uint32_t>(quad * 32) << 16) +
-                                   static_cast<uint32_t>(acc * BN);
-            uint16_t *dst = args.out + static_cast<size_t>(t) * args.N + nt * BN;
-#pragma unroll 1
-            for (int cb = 0; cb < BN; cb += 32) {
-                uint32_t yr[32];
-                tmem_ld32(taddr + cb, yr);
-                tmem_ld_wait();
-                tmem_st32(taddr + cb, z);
-                if (t < T) {
-#pragma unroll
-                    for (int q = 0; q < 4; ++q)
-                        st_global_cs_v4(dst + cb + 8 * q,
-                                        pack_bf16x2(__uint_as_float(yr[8 * q + 0]), __uint_as_float(yr[8 * q + 1])),
-                                        pack_bf16x2(__uint_as_float(yr[8 * q + 2]), __uint_as_float(yr[8 * q + 3])),
-                                        pack_bf16x2(__uint_as_float(yr[8 * q + 4]), __uint_as_float(yr[8 * q + 5])),
-                                        pack_bf16x2(__uint_as_float(yr[8 * q + 6]), __uint_as_float(yr[8 * q + 7])));
-                }
-            }
-            tmem_st_wait();
-            tc_fence_before();
-            __syncwarp();
-            if (lane == 0) mbar_arrive_cluster(tempty_even + 8u * acc);
-            if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
-        }
-    }
-
-    tc_fence_before();
-    __syncthreads();
-    cluster_sync();  // the even CTA's MMAs read this CTA's shared memory until here
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc_pair(tmem_base, C::TMEM_COLS);
-    }
-}
-
-template <int BN>
-cudaError_t launch_pair_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a,
-                          int num_sms, cudaStream_t s) {
-    using C = KPairCfg<BN>;
-    auto kern = gemm_k_pair_kernel<BN>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
-    if (e != cudaSuccess) return e;
-    const int m_tiles = (a.T + 2 * BM - 1) / (2 * BM);
-    const int items = m_tiles * (a.N / BN);
-    int pairs = num_sms / 2;
-    if (pairs > items) pairs = items;
-    kern<<<2 * pairs, kThreads, C::SMEM_BYTES, s>>>(tmA, tmB, a);
-    return cudaGetLastError();
-}
-
 }  // namespace
 
 int gemm_k_max_groups() { return kMaxKGroups; }
-int gemm_k_pair_max_groups() { return kMaxPairGroups; }
 
-cudaError_t launch_gemm_k_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a,
-                               int num_sms, cudaStream_t s) {
-    return launch_pair_t<256>(tmA, tmB, a, num_sms, s);
-}
 
 cudaError_t launch_gemm_k(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a,
                           int num_sms, cudaStream_t s) {

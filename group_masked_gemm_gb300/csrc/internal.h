@@ -52,12 +52,10 @@ cudaError_t launch_gemm_mn(MNMode mode, int bn, const CUtensorMap &tmB0, const C
 cudaError_t launch_gemm_k(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
                           const KArgs &a, int num_sms, cudaStream_t s);
 
-// CTA-pair GEMM-K (256 tokens x 256 columns per pair): tmA box 64 x 128,
-// tmB box 64 x 128 (each CTA loads half of the pair's 256 weight rows).
-cudaError_t launch_gemm_k_pair(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a,
-                               int num_sms, cudaStream_t s);
-
 cudaError_t launch_decode_mn(MNMode mode, const DecodeArgs &a, int num_sms, cudaStream_t s);
-cudaError_t launch_decode_k(const DecodeArgs &a, int num_sms, cudaStream_t s);
+// ws: fp32 partial sums, decode_k_workspace_bytes(T, K, N, G) bytes.
+cudaError_t launch_decode_k(const DecodeArgs &a, float *ws, cudaStream_t s);
+size_t decode_k_workspace_bytes(int T, int K, int N, int G);
+size_t decode_mn_smem_bytes(int T, int K, int n_groups);
 
 }  // namespace wide
