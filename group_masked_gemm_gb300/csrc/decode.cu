@@ -308,3 +308,77 @@ cudaError_t launch_decode_k(const DecodeArgs &a, float *ws, cudaStream_t s) {
 }
 
 }  // namespace wide
+
+// ---------------------------------------------------------------------------
+// Allocation-free decode GEMM-K.
+//
+// Some callers of this library cannot allocate device memory: code running
+// under a memory planner that owns every device allocation, plugin hosts that
+// hand a kernel no workspace, or paths where a cudaMalloc (which can
+// synchronise the device) is not acceptable.  For them the decode GEMM-K
+// keeps its fp32 partial sums in this fixed array instead of a caller
+// workspace.  It is part of the module, so every GPU that loads the library
+// holds it until the process exits.
+#include <mutex>
+
+#include "../../include/wide.h"
+
+namespace {
+
+constexpr size_t kStaticScratchBytes = WIDE_NOALLOC_SCRATCH_BYTES;
+static __device__ __align__(256) float g_static_scratch[kStaticScratchBytes / sizeof(float)];
+
+constexpr int kMaxStaticDevices = 64;
+std::mutex g_static_mutex;
+float *g_static_scratch_ptr[kMaxStaticDevices] = {nullptr};
+int g_static_num_sms[kMaxStaticDevices] = {0};
+
+// Device address of g_static_scratch on the current device.  The first call
+// on each device looks it up (cudaGetSymbolAddress) and caches it.
+wide_status_t static_scratch_for_current_device(float **ptr, int *num_sms) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxStaticDevices)
+        return WIDE_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_static_mutex);
+    if (g_static_scratch_ptr[dev] == nullptr) {
+        float *p = nullptr;
+        if (cudaGetSymbolAddress(reinterpret_cast<void **>(&p), g_static_scratch) != cudaSuccess ||
+            p == nullptr)
+            return WIDE_ERR_CUDA;
+        int n = 0;
+        if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+            return WIDE_ERR_CUDA;
+        g_static_scratch_ptr[dev] = p;
+        g_static_num_sms[dev] = n;
+    }
+    *ptr = g_static_scratch_ptr[dev];
+    *num_sms = g_static_num_sms[dev];
+    return WIDE_OK;
+}
+
+bool aligned16_ptr(const void *p) {
+    return p != nullptr && (reinterpret_cast<uintptr_t>(p) & 15u) == 0;
+}
+
+}  // namespace
+
+extern "C" wide_status_t wide_gemm_k_decode_noalloc(const uint16_t *A, const uint16_t *W,
+                                                    const uint8_t *mask, int T, int K, int N,
+                                                    int G, uint16_t *Y, void *stream) {
+    if (!aligned16_ptr(A) || !aligned16_ptr(W) || !aligned16_ptr(mask) || !aligned16_ptr(Y))
+        return WIDE_ERR_INVALID_ARG;
+    if (T < 1 || T > 16 || K < 64 || N < 64 || K % 64 || N % 64) return WIDE_ERR_INVALID_ARG;
+    if (!(G == 64 || G == 128 || G == 256 || G == 512))
+        return (G >= 16 && (G & (G - 1)) == 0) ? WIDE_ERR_UNSUPPORTED : WIDE_ERR_INVALID_ARG;
+    if (K % G) return WIDE_ERR_INVALID_ARG;
+    if (wide::decode_k_workspace_bytes(T, K, N, G) > kStaticScratchBytes) return WIDE_ERR_WORKSPACE;
+    float *scratch = nullptr;
+    int num_sms = 0;
+    wide_status_t st = static_scratch_for_current_device(&scratch, &num_sms);
+    if (st != WIDE_OK) return st;
+    (void)num_sms;
+    wide::DecodeArgs a{A, W, nullptr, mask, Y, T, K, N, G};
+    return wide::launch_decode_k(a, scratch, static_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? WIDE_OK
+               : WIDE_ERR_CUDA;
+}

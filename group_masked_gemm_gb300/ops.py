@@ -59,8 +59,10 @@ def lib():
                 L.wide_gemm_k_workspace_size.argtypes = [i, i, i, i]
                 L.wide_gemm_k_workspace_size.restype = sz
                 L.wide_device_status.argtypes = [p]
+                L.wide_gemm_k_decode_noalloc.argtypes = [p, p, p, i, i, i, i, p, p]
                 for fn in ("wide_reorder_masks", "wide_gemm_mn_gate_up", "wide_gemm_k_down",
-                           "wide_proj_mn", "wide_proj_k", "wide_device_status"):
+                           "wide_proj_mn", "wide_proj_k", "wide_device_status",
+                           "wide_gemm_k_decode_noalloc"):
                     getattr(L, fn).restype = i
                 _lib = L
     return _lib
@@ -183,6 +185,22 @@ def proj_k(A, W, mask, perm, counts, G, out=None, ws=None, stream=None):
     _check("wide_proj_k", lib().wide_proj_k(
         _ptr(A), _ptr(W), _ptr(mask), _ptr(perm), _ptr(counts), T, K, N, G,
         _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
+    return out
+
+
+def gemm_k_decode_noalloc(A, W, mask, G, out=None, stream=None):
+    """Decode (T <= 16) GEMM-K through the allocation-free entry point: the
+    library keeps the partial sums in its own fixed device array, so the
+    call itself allocates nothing (``out`` may be preallocated too)."""
+    _need(A, torch.bfloat16, "A", 2)
+    _need(W, torch.bfloat16, "W", 2)
+    _need(mask, torch.uint8, "mask", 2)
+    T, K = A.shape
+    N = W.shape[0]
+    if out is None:
+        out = torch.empty((T, N), dtype=torch.bfloat16, device=A.device)
+    _check("wide_gemm_k_decode_noalloc", lib().wide_gemm_k_decode_noalloc(
+        _ptr(A), _ptr(W), _ptr(mask), T, K, N, G, _ptr(out), _stream(stream)))
     return out
 
 

@@ -140,6 +140,35 @@ wide_status_t wide_proj_k(const uint16_t *A, const uint16_t *W,
 size_t wide_gemm_k_workspace_size(int T, int K, int N, int G);
 
 /*
+ * Allocation-free decode GEMM-K (T <= 16).  No counterpart in the paper: an
+ * addition of this library for callers that cannot allocate device memory
+ * (a memory planner that owns every device allocation, a plugin host that
+ * provides no workspace, or a path where a cudaMalloc would synchronise).
+ *
+ * Computes exactly what wide_gemm_k_down / wide_proj_k compute for T <= 16:
+ *   Y[t, n] = sum_g M[t,g] sum_{k in [gG,(g+1)G)} A[t,k] W[n,k]
+ * (A: bf16 [T, K]; W: bf16 [N, K]; mask: uint8 [T, K/G]; Y: bf16 [T, N]),
+ * with the same kernels and the same result, but its fp32 partial sums live
+ * in a fixed array of WIDE_NOALLOC_SCRATCH_BYTES inside the library (held by
+ * every GPU that loads the library until the process exits) instead of a
+ * caller workspace.  Nothing is allocated or freed by this call.
+ *   - Sizes whose partial sums (splits x T x N x 4 bytes; 1.3 MB for
+ *     T = 16, K = 14336, N = 4096, G = 128) exceed the array return
+ *     WIDE_ERR_WORKSPACE; T > 16 returns WIDE_ERR_INVALID_ARG.
+ *   - The first call on each device looks up the array's device address
+ *     (cudaGetSymbolAddress) and caches it; make that first call before any
+ *     stream capture on that device.
+ *   - Every call shares the one array; the partial sums of a call are fully
+ *     written before they are read, so nothing needs clearing between
+ *     calls.  Calls whose kernels overlap on the GPU (e.g. issued on two
+ *     streams without ordering) race on the array: order them on one stream.
+ */
+#define WIDE_NOALLOC_SCRATCH_BYTES (4u << 20)
+wide_status_t wide_gemm_k_decode_noalloc(const uint16_t *A, const uint16_t *W,
+                                         const uint8_t *mask, int T, int K, int N, int G,
+                                         uint16_t *Y, void *stream);
+
+/*
  * Device status word: synchronises `stream`, returns WIDE_OK or the first
  * device-side failure recorded since the last call (WIDE_ERR_TIMEOUT), and
  * clears it.  This is the only call that synchronises.
