@@ -4,6 +4,7 @@
 // word.  No call allocates, frees or synchronises (except wide_device_status).
 #include <cudaTypedefs.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "../../include/wide.h"
@@ -89,6 +90,17 @@ wide_status_t encode_bf16_2d(CUtensorMap *m, const void *base, long long rows, l
     return r == CUDA_SUCCESS ? WIDE_OK : WIDE_ERR_CUDA;
 }
 
+// Decode kernels: tensor-core path unless WIDE_DECODE_TC=0 (temporary A/B switch).
+bool decode_tc() {
+    static const bool v = [] {
+        const char *e = std::getenv("WIDE_DECODE_TC");
+        return !(e != nullptr && e[0] == '0');
+    }();
+    return v;
+}
+
+bool decode_k_uses_tc(int N) { return decode_tc() && N % 128 == 0; }
+
 // Shared validation of GEMM-MN style calls; out features N grouped by G.
 wide_status_t check_mn(const void *X, const void *W0, const void *W1, const void *mask,
                        const void *perm, const void *counts, int T, int K, int N, int G,
@@ -129,6 +141,16 @@ wide_status_t run_mn(wide::MNMode mode, const uint16_t *X, const uint16_t *W0,
     if (st != WIDE_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool gate_up = mode == wide::MNMode::kGateUp;
+    if (T <= kDecodeMaxT && decode_tc()) {
+        const int rt = wide::decode_tc_rows_per_item();
+        CUtensorMap tmW0, tmW1, tmX;
+        if ((st = encode_bf16_2d(&tmW0, W0, N, K, rt)) != WIDE_OK) return st;
+        if ((st = encode_bf16_2d(&tmW1, gate_up ? W1 : W0, N, K, rt)) != WIDE_OK) return st;
+        if ((st = encode_bf16_2d(&tmX, X, T, K, T < 16 ? T : 16)) != WIDE_OK) return st;
+        wide::DecodeArgs a{X, W0, gate_up ? W1 : nullptr, mask, out, T, K, N, G};
+        return from_cuda(
+            wide::launch_decode_mn_tc(mode, tmW0, tmW1, tmX, a, ctx.status, ctx.num_sms, s));
+    }
     if (T <= kDecodeMaxT && wide::decode_mn_smem_bytes(T, K, N / G) <= 200 * 1024) {
         wide::DecodeArgs a{X, W0, gate_up ? W1 : nullptr, mask, out, T, K, N, G};
         return from_cuda(wide::launch_decode_mn(mode, a, ctx.num_sms, s));
@@ -154,6 +176,14 @@ wide_status_t run_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask, i
     wide_status_t st = device_ctx(&ctx);
     if (st != WIDE_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
+    if (T <= kDecodeMaxT && decode_k_uses_tc(N)) {
+        CUtensorMap tmW, tmA;
+        if ((st = encode_bf16_2d(&tmW, W, N, K, 128)) != WIDE_OK) return st;
+        if ((st = encode_bf16_2d(&tmA, A, T, K, T < 16 ? T : 16)) != WIDE_OK) return st;
+        wide::DecodeArgs a{A, W, nullptr, mask, out, T, K, N, G};
+        return from_cuda(
+            wide::launch_decode_k_tc(tmW, tmA, a, static_cast<float *>(ws), ctx.status, s));
+    }
     if (T <= kDecodeMaxT) {
         wide::DecodeArgs a{A, W, nullptr, mask, out, T, K, N, G};
         return from_cuda(wide::launch_decode_k(a, static_cast<float *>(ws), s));
@@ -228,7 +258,8 @@ size_t wide_gemm_k_workspace_size(int T, int K, int N, int G) {
     // Prefill (T > 16) reduces in TMEM and needs none; the decode path sums
     // fp32 partials of the split reduction dimension.
     if (T < 1 || T > kDecodeMaxT || G <= 0 || K < G || K % G) return 0;
-    return wide::decode_k_workspace_bytes(T, K, N, G);
+    return decode_k_uses_tc(N) ? wide::decode_tc_k_workspace_bytes(T, K, N, G)
+                               : wide::decode_k_workspace_bytes(T, K, N, G);
 }
 
 wide_status_t wide_gemm_k_down(const uint16_t *H, const uint16_t *W_down, const uint8_t *mask,

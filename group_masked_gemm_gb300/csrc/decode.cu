@@ -293,6 +293,12 @@ static cudaError_t launch_k_partial(const DecodeArgs &a, int gps, int splits, fl
     return cudaGetLastError();
 }
 
+cudaError_t launch_decode_k_finalize(const float *ws, int splits, int TN, uint16_t *out,
+                                     cudaStream_t s) {
+    decode_k_finalize_kernel<<<(TN + kThreads - 1) / kThreads, kThreads, 0, s>>>(ws, splits, TN, out);
+    return cudaGetLastError();
+}
+
 cudaError_t launch_decode_k(const DecodeArgs &a, float *ws, cudaStream_t s) {
     const int ng = a.K / a.G;
     const int gps = decode_k_groups_per_split(a.T, a.K, a.G);

@@ -57,5 +57,19 @@ cudaError_t launch_decode_mn(MNMode mode, const DecodeArgs &a, int num_sms, cuda
 cudaError_t launch_decode_k(const DecodeArgs &a, float *ws, cudaStream_t s);
 size_t decode_k_workspace_bytes(int T, int K, int N, int G);
 size_t decode_mn_smem_bytes(int T, int K, int n_groups);
+cudaError_t launch_decode_k_finalize(const float *ws, int splits, int TN, uint16_t *out,
+                                     cudaStream_t s);
+
+// Tensor-core decode (T <= 16): weight rows on the MMA's M side, tokens on N.
+// tmW0/tmW1: weight maps, box 64 x decode_tc_rows_per_item(); tmX: token rows
+// [T, K], box 64 x min(T, 16).  GEMM-K: tmW box 64 x 128 (N % 128 == 0),
+// tmA: the token rows [T, K], box 64 x min(T, 16).
+int decode_tc_rows_per_item();
+size_t decode_tc_k_workspace_bytes(int T, int K, int N, int G);
+cudaError_t launch_decode_mn_tc(MNMode mode, const CUtensorMap &tmW0, const CUtensorMap &tmW1,
+                                const CUtensorMap &tmX, const DecodeArgs &a, int *status,
+                                int num_sms, cudaStream_t s);
+cudaError_t launch_decode_k_tc(const CUtensorMap &tmW, const CUtensorMap &tmA, const DecodeArgs &a,
+                               float *ws, int *status, cudaStream_t s);
 
 }  // namespace wide
