@@ -75,6 +75,17 @@ wide_status_t device_ctx(DeviceCtx *ctx) {
     return WIDE_OK;
 }
 
+// SM count that sizes the decode GEMM-K split (and so its workspace): the
+// current device's, or 152 (GB300) when no device is visible.
+int sizing_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) == cudaSuccess &&
+        cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) == cudaSuccess && n > 0)
+        return n;
+    (void)cudaGetLastError();
+    return 152;
+}
+
 // 2-D bf16 tensor [rows, cols] (cols contiguous), box {64 cols, box_rows},
 // 128-byte swizzle; out-of-range elements read as zero.
 wide_status_t encode_bf16_2d(CUtensorMap *m, const void *base, long long rows, long long cols,
@@ -90,16 +101,13 @@ wide_status_t encode_bf16_2d(CUtensorMap *m, const void *base, long long rows, l
     return r == CUDA_SUCCESS ? WIDE_OK : WIDE_ERR_CUDA;
 }
 
-// Decode kernels: tensor-core path unless WIDE_DECODE_TC=0 (temporary A/B switch).
-bool decode_tc() {
-    static const bool v = [] {
-        const char *e = std::getenv("WIDE_DECODE_TC");
-        return !(e != nullptr && e[0] == '0');
-    }();
-    return v;
-}
+// Decode (T <= 16) kernels, chosen by measurement on GB300 (8B FFN shapes):
+// gate/up and q_proj stream weight rows on the CUDA cores up to 4 tokens and
+// on the tensor cores above; down/o_proj run the GEMM-K kernel with the
+// groups split over CTAs whenever N is a multiple of its 128-column tile.
+constexpr int kDecodeMnCudaMaxT = 4;
 
-bool decode_k_uses_tc(int N) { return decode_tc() && N % 128 == 0; }
+bool decode_k_on_gemm_k(int N) { return N % 128 == 0; }
 
 // Shared validation of GEMM-MN style calls; out features N grouped by G.
 wide_status_t check_mn(const void *X, const void *W0, const void *W1, const void *mask,
@@ -141,7 +149,11 @@ wide_status_t run_mn(wide::MNMode mode, const uint16_t *X, const uint16_t *W0,
     if (st != WIDE_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
     const bool gate_up = mode == wide::MNMode::kGateUp;
-    if (T <= kDecodeMaxT && decode_tc()) {
+    if (T <= kDecodeMnCudaMaxT && wide::decode_mn_smem_bytes(T, K, N / G) <= 200 * 1024) {
+        wide::DecodeArgs a{X, W0, gate_up ? W1 : nullptr, mask, out, T, K, N, G};
+        return from_cuda(wide::launch_decode_mn(mode, a, ctx.num_sms, s));
+    }
+    if (T <= kDecodeMaxT) {
         const int rt = wide::decode_tc_rows_per_item();
         CUtensorMap tmW0, tmW1, tmX;
         if ((st = encode_bf16_2d(&tmW0, W0, N, K, rt)) != WIDE_OK) return st;
@@ -150,10 +162,6 @@ wide_status_t run_mn(wide::MNMode mode, const uint16_t *X, const uint16_t *W0,
         wide::DecodeArgs a{X, W0, gate_up ? W1 : nullptr, mask, out, T, K, N, G};
         return from_cuda(
             wide::launch_decode_mn_tc(mode, tmW0, tmW1, tmX, a, ctx.status, ctx.num_sms, s));
-    }
-    if (T <= kDecodeMaxT && wide::decode_mn_smem_bytes(T, K, N / G) <= 200 * 1024) {
-        wide::DecodeArgs a{X, W0, gate_up ? W1 : nullptr, mask, out, T, K, N, G};
-        return from_cuda(wide::launch_decode_mn(mode, a, ctx.num_sms, s));
     }
     if (perm == nullptr || counts == nullptr) return WIDE_ERR_INVALID_ARG;
     const int bn = gate_up ? (G == 64 ? 64 : 128) : (G == 64 ? 64 : G == 128 ? 128 : 256);
@@ -176,13 +184,14 @@ wide_status_t run_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask, i
     wide_status_t st = device_ctx(&ctx);
     if (st != WIDE_OK) return st;
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    if (T <= kDecodeMaxT && decode_k_uses_tc(N)) {
-        CUtensorMap tmW, tmA;
-        if ((st = encode_bf16_2d(&tmW, W, N, K, 128)) != WIDE_OK) return st;
+    if (T <= kDecodeMaxT && decode_k_on_gemm_k(N)) {
+        CUtensorMap tmA, tmB;
         if ((st = encode_bf16_2d(&tmA, A, T, K, T < 16 ? T : 16)) != WIDE_OK) return st;
-        wide::DecodeArgs a{A, W, nullptr, mask, out, T, K, N, G};
+        if ((st = encode_bf16_2d(&tmB, W, N, K, 128)) != WIDE_OK) return st;
+        wide::KArgs a{mask, out, T, K, N, G, ctx.status};
+        a.a_rows = T < 16 ? T : 16;
         return from_cuda(
-            wide::launch_decode_k_tc(tmW, tmA, a, static_cast<float *>(ws), ctx.status, s));
+            wide::launch_gemm_k_decode(tmA, tmB, a, static_cast<float *>(ws), ctx.num_sms, s));
     }
     if (T <= kDecodeMaxT) {
         wide::DecodeArgs a{A, W, nullptr, mask, out, T, K, N, G};
@@ -258,8 +267,8 @@ size_t wide_gemm_k_workspace_size(int T, int K, int N, int G) {
     // Prefill (T > 16) reduces in TMEM and needs none; the decode path sums
     // fp32 partials of the split reduction dimension.
     if (T < 1 || T > kDecodeMaxT || G <= 0 || K < G || K % G) return 0;
-    return decode_k_uses_tc(N) ? wide::decode_tc_k_workspace_bytes(T, K, N, G)
-                               : wide::decode_k_workspace_bytes(T, K, N, G);
+    return decode_k_on_gemm_k(N) ? wide::gemm_k_decode_workspace_bytes(T, K, N, G, sizing_sms())
+                                 : wide::decode_k_workspace_bytes(T, K, N, G);
 }
 
 wide_status_t wide_gemm_k_down(const uint16_t *H, const uint16_t *W_down, const uint8_t *mask,

@@ -1,6 +1,6 @@
-// decode_tc.cu -- small-T (decode) group-masked projections on tcgen05
-// (WIDE, App. B: GEMV variants of GEMM-MN and GEMM-K; in decoding the mask
-// reordering is bypassed and routing is checked at block level).
+// decode_tc.cu -- small-T (decode) GEMM-MN on tcgen05 (WIDE, App. B: GEMV
+// variant of GEMM-MN; in decoding the mask reordering is bypassed and routing
+// is checked at block level).
 //
 // Decode is bound by HBM reads of the weight groups some token uses.  The
 // products are computed transposed, D[row, token] = sum_k W[row,k] X[token,k],
@@ -12,11 +12,8 @@
 //                 write zeros and never read their weights.  For gate/up the
 //                 A tile holds the 32 gate rows in rows 0..31 and the 32 up
 //                 rows in rows 64..95, so one MMA computes both.
-//   decode_k_tc : one CTA per (128-row tile of W, split of the groups); the
-//                 split's token rows are staged once, masked, in the MMA's B
-//                 layout; only k-blocks of groups some token uses are
-//                 streamed; fp32 partials go to the workspace and the
-//                 finalize kernel sums them in split order.
+// It serves 5 <= T <= 16; smaller batches go to the CUDA-core kernel of
+// decode.cu, which streams the same bytes with less issue overhead.
 #include "common.cuh"
 #include "internal.h"
 
@@ -38,10 +35,6 @@ constexpr int SCRATCH_BYTES = 128 * (NTOK + 1) * 4;
 // TMEM: two fp32 accumulators of NTOK columns (double-buffered across items)
 constexpr int MN_SMEM = 1024 + MN_STAGES * MN_STAGE_BYTES + SCRATCH_BYTES + 256;
 static_assert(2 * MN_SMEM <= 227 * 1024, "two decode_mn_tc CTAs per SM");
-
-constexpr int K_STAGES = 6;
-constexpr int kTokBlockBytes = 96 * 1024;  // staged token rows of one split
-constexpr int K_SMEM = 1024 + K_STAGES * A_BYTES + kTokBlockBytes + 2048 + 256;
 
 __device__ __forceinline__ uint16_t to_bf16_bits(float f) {
     __nv_bfloat16 h = __float2bfloat16_rn(f);
@@ -224,157 +217,6 @@ __global__ void __launch_bounds__(kTcThreads)
     }
 }
 
-// One (128-row tile of W, split of the groups) of the decode GEMM-K.
-__global__ void __launch_bounds__(kTcThreads, 1)
-    decode_k_tc_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmA,
-                       const DecodeArgs a, int gps, float *ws, int *status) {
-    extern __shared__ __align__(1024) uint8_t smem_raw[];
-    uint8_t *smem = reinterpret_cast<uint8_t *>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint8_t *stages = smem;
-    uint8_t *tok = smem + K_STAGES * A_BYTES;                       // [kb][16 rows][128 B]
-    uint32_t *gbits = reinterpret_cast<uint32_t *>(tok + kTokBlockBytes);  // [gps]
-    uint64_t *bars = reinterpret_cast<uint64_t *>(tok + kTokBlockBytes + 2048);
-    uint64_t *full = bars, *empty = bars + K_STAGES, *tfull = bars + 2 * K_STAGES;
-    uint64_t *tok_ready = tfull + 1;   // token block masked and visible to the MMA (4 warps)
-    uint64_t *tok_loaded = tok_ready + 1;  // TMA of the token block landed
-    uint32_t *s_tmem = reinterpret_cast<uint32_t *>(tok_loaded + 1);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int T = a.T, K = a.K, N = a.N, G = a.G;
-    const int ng = K / G;
-    const int n0 = blockIdx.x * 128;
-    const int g_begin = blockIdx.y * gps;
-    const int g_end = min(ng, g_begin + gps);
-    const int k0 = g_begin * G;
-    const int nkb = (g_end - g_begin) * G / BK;
-    const int kb_per_g = G / BK;
-
-    // tokens active per group of this split
-    for (int gi = threadIdx.x; gi < g_end - g_begin; gi += kTcThreads) {
-        uint32_t b = 0;
-        for (int t = 0; t < T; ++t) b |= static_cast<uint32_t>(a.mask[t * ng + g_begin + gi] != 0) << t;
-        gbits[gi] = b;
-    }
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < K_STAGES; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
-        }
-        mbar_init(tfull, 1);
-        mbar_init(tok_ready, 4);
-        mbar_init(tok_loaded, 1);
-        fence_barrier_init();
-    }
-    if (warp == 1) {
-        tmem_alloc(s_tmem, TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem_base = *s_tmem;
-    int n_live = 0;
-    for (int gi = 0; gi < g_end - g_begin; ++gi) n_live += gbits[gi] != 0u;
-
-    const int trows = T < NTOK ? T : NTOK;
-    if (warp == 0) {
-        if (lane == 0) {
-            prefetch_tmap(&tmW);
-            // token rows of the live k-blocks: one min(T,16)-row box each, straight
-            // into the B operand's swizzled 2 KB slot (rows >= T stay stale and
-            // only feed output columns that are never stored)
-            int n_live_kb = 0;
-            for (int kb = 0; kb < nkb; ++kb) n_live_kb += gbits[kb / kb_per_g] != 0u;
-            mbar_arrive_expect_tx(tok_loaded, static_cast<uint32_t>(n_live_kb * trows * BK * 2));
-            for (int kb = 0; kb < nkb; ++kb)
-                if (gbits[kb / kb_per_g] != 0u)
-                    tma_load_2d(tok + kb * XB_BYTES, &tmA, tok_loaded, k0 + kb * BK, 0);
-            int stage = 0;
-            uint32_t phase = 0, used = 0, last_parity = 0;
-            bool ok = true;
-            for (int kb = 0; kb < nkb && ok; ++kb) {
-                if (gbits[kb / kb_per_g] == 0u) continue;  // no token uses this group
-                if (!mbar_wait(&empty[stage], phase ^ 1u, status)) { ok = false; break; }
-                mbar_arrive_expect_tx(&full[stage], A_BYTES);
-                tma_load_2d(stages + stage * A_BYTES, &tmW, &full[stage], k0 + kb * BK, n0);
-                used |= 1u << stage;
-                last_parity = (last_parity & ~(1u << stage)) | (phase << stage);
-                if (++stage == K_STAGES) { stage = 0; phase ^= 1u; }
-            }
-            for (int s = 0; s < K_STAGES; ++s)
-                if (used & (1u << s)) mbar_wait(&full[s], (last_parity >> s) & 1u, status);
-            mbar_wait(tok_loaded, 0, status);
-        }
-        __syncwarp();
-    } else if (warp == 1) {
-        if (lane == 0) {
-            int stage = 0;
-            uint32_t phase = 0;
-            bool first = true;
-            const bool staged = mbar_wait(tok_ready, 0, status);
-            for (int kb = 0; kb < nkb && staged; ++kb) {
-                if (gbits[kb / kb_per_g] == 0u) continue;
-                if (!mbar_wait(&full[stage], phase, status)) break;
-                tc_fence_after();
-                const uint32_t a0 = smem_u32(stages + stage * A_BYTES);
-                const uint32_t x0 = smem_u32(tok + kb * XB_BYTES);
-#pragma unroll
-                for (int kk = 0; kk < BK / 16; ++kk) {
-                    mma_bf16(tmem_base, sw128_kmajor_desc(a0 + kk * 32), sw128_kmajor_desc(x0 + kk * 32),
-                             IDESC, first ? 0u : 1u);
-                    first = false;
-                }
-                mma_commit(&empty[stage]);
-                if (++stage == K_STAGES) { stage = 0; phase ^= 1u; }
-            }
-            mma_commit(tfull);
-            mbar_wait(tfull, 0, status);
-        }
-        __syncwarp();
-    } else {
-        // Warps 2..5 mask the token block once its copies have landed: in
-        // each live k-block, the rows of tokens that do not use that group are
-        // zeroed (16 bytes per thread and step), so they contribute nothing.
-        int tl = 1;
-        if (lane == 0) tl = mbar_wait(tok_loaded, 0, status);
-        tl = __shfl_sync(0xffffffffu, tl, 0);
-        const int n_chunks = tl ? nkb * trows * 8 : 0;
-        for (int i = threadIdx.x - 64; i < n_chunks; i += 128) {
-            const int kb = i / (trows * 8);
-            const int rem = i - kb * trows * 8;
-            const int t = rem >> 3, c = rem & 7;
-            const uint32_t gb = gbits[kb / kb_per_g];
-            if (gb != 0u && !((gb >> t) & 1u))
-                *reinterpret_cast<uint4 *>(tok + kb * XB_BYTES + t * 128 + c * 16) = make_uint4(0, 0, 0, 0);
-        }
-        fence_proxy_async_smem();  // generic-proxy writes -> tensor-core (async proxy) reads
-        __syncwarp();
-        if (lane == 0) mbar_arrive(tok_ready);
-
-        const int quad = warp & 3;
-        const int r = quad * 32 + lane;
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(tfull, 0, status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        tc_fence_after();
-        uint32_t v[16];
-        tmem_ld16(tmem_base + (static_cast<uint32_t>(quad * 32) << 16), v);
-        tmem_ld_wait();
-        float *out = ws + static_cast<size_t>(blockIdx.y) * T * N;
-#pragma unroll
-        for (int t = 0; t < NTOK; ++t)
-            if (t < T)
-                out[static_cast<size_t>(t) * N + n0 + r] = (ok && n_live > 0) ? __uint_as_float(v[t]) : 0.f;
-    }
-    tc_fence_before();
-    __syncthreads();
-    if (warp == 1) {
-        tc_fence_after();
-        tmem_dealloc(tmem_base, TMEM_COLS);
-    }
-}
-
 template <MNMode MODE>
 cudaError_t launch_mn(const CUtensorMap &tmW0, const CUtensorMap &tmW1, const CUtensorMap &tmX,
                       const DecodeArgs &a, int *status, int num_sms, cudaStream_t s) {
@@ -391,41 +233,12 @@ cudaError_t launch_mn(const CUtensorMap &tmW0, const CUtensorMap &tmW1, const CU
 
 int decode_tc_rows_per_item() { return RT; }
 
-int decode_tc_groups_per_split(int K, int G) {
-    const int ng = K / G;
-    int gps_max = kTokBlockBytes / (NTOK * G * 2);
-    if (gps_max < 1) gps_max = 1;
-    const int splits = (ng + gps_max - 1) / gps_max;
-    return (ng + splits - 1) / splits;
-}
-
-size_t decode_tc_k_workspace_bytes(int T, int K, int N, int G) {
-    const int ng = K / G;
-    const int gps = decode_tc_groups_per_split(K, G);
-    const int splits = (ng + gps - 1) / gps;
-    return static_cast<size_t>(splits) * T * N * sizeof(float);
-}
-
 cudaError_t launch_decode_mn_tc(MNMode mode, const CUtensorMap &tmW0, const CUtensorMap &tmW1,
                                 const CUtensorMap &tmX, const DecodeArgs &a, int *status,
                                 int num_sms, cudaStream_t s) {
     if (mode == MNMode::kGateUp)
         return launch_mn<MNMode::kGateUp>(tmW0, tmW1, tmX, a, status, num_sms, s);
     return launch_mn<MNMode::kPlain>(tmW0, tmW1, tmX, a, status, num_sms, s);
-}
-
-cudaError_t launch_decode_k_tc(const CUtensorMap &tmW, const CUtensorMap &tmA, const DecodeArgs &a,
-                               float *ws, int *status, cudaStream_t s) {
-    cudaError_t e = cudaFuncSetAttribute(decode_k_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         K_SMEM);
-    if (e != cudaSuccess) return e;
-    const int ng = a.K / a.G;
-    const int gps = decode_tc_groups_per_split(a.K, a.G);
-    const int splits = (ng + gps - 1) / gps;
-    decode_k_tc_kernel<<<dim3(a.N / 128, splits), kTcThreads, K_SMEM, s>>>(tmW, tmA, a, gps, ws, status);
-    e = cudaGetLastError();
-    if (e != cudaSuccess) return e;
-    return launch_decode_k_finalize(ws, splits, a.T * a.N, a.out, s);
 }
 
 }  // namespace wide

@@ -18,6 +18,16 @@
 // tile's mask block into lane masks and a list of live groups, double
 // buffered), 3..6 epilogue (TMEM -> bf16 rows of Y, then re-zeroes the
 // accumulator for its next tile).
+//
+// Decode (T <= 16) runs the same kernel with a 16-row token stage (AR = 16):
+// a stage holds 2 KB of tokens and 16 KB of weights, so 11 stages of weights
+// are in flight per SM.  The M = 128 MMA still reads 128 A rows; rows 16..127
+// fall inside the same stage's weight tile and land in TMEM lanes that the
+// lane mask disables (tokens >= T are inactive in every group).  The groups
+// live for some token are dealt in equal contiguous shares to `splits` work
+// items per output tile (so a sparse mask does not leave a few CTAs with most
+// of the live weights); each item writes fp32 partial sums, added in split
+// order by a finalize kernel.
 #include "common.cuh"
 #include "internal.h"
 
@@ -30,37 +40,69 @@ constexpr int kThreads = 224;
 constexpr int kMaxKGroups = 512;
 constexpr int kSmemBudget = 225 * 1024;
 
-template <int BN>
+template <int BN, int AR>
 struct KCfg {
-    static constexpr int A_BYTES = BM * BK * 2;
+    static_assert(AR == BM || AR == 16, "token stage rows");
+    static constexpr int A_BYTES = AR * BK * 2;
     static constexpr int B_BYTES = BN * BK * 2;
     static constexpr int STAGE_BYTES = A_BYTES + B_BYTES;
     // per mask buffer: lane masks [ng][4] + live-group list [ng] + count
     static constexpr int MASK_BUF_BYTES = kMaxKGroups * 16 + kMaxKGroups * 4 + 16;
-    static constexpr int BAR_BYTES = 256;
+    static constexpr int BAR_BYTES = 512;
     static constexpr int STAGES_FIT =
         (kSmemBudget - 1024 - 2 * MASK_BUF_BYTES - BAR_BYTES) / STAGE_BYTES;
-    static constexpr int STAGES = STAGES_FIT > 8 ? 8 : STAGES_FIT;
+    static constexpr int MAX_STAGES = AR == BM ? 8 : 12;
+    static constexpr int STAGES = STAGES_FIT > MAX_STAGES ? MAX_STAGES : STAGES_FIT;
     static constexpr int TMEM_COLS = (2 * BN <= 256) ? 256 : 512;
     static constexpr uint32_t IDESC = idesc_bf16_f32(BM, BN);
     static constexpr int SMEM_BYTES = 1024 + STAGES * STAGE_BYTES + 2 * MASK_BUF_BYTES + BAR_BYTES;
     static_assert(STAGES >= 2, "pipeline needs two stages");
+    static_assert((2 * STAGES + 9) * 8 + 8 <= BAR_BYTES, "barrier area");
+    static_assert(STAGE_BYTES % 1024 == 0 && A_BYTES % 1024 == 0, "SW128 operand alignment");
     static_assert(SMEM_BYTES <= 227 * 1024, "shared memory budget");
 };
 
 // Mask buffer b (of 2) inside the mask area: lane masks [ng][4], the live
-// group list [ng] and its length.
+// group list [ng], and the slice live[first, first + n_live) of this item.
 struct MaskBuf {
     uint32_t *lanes;  // [ng][4] disable-output-lane words
     int *live;        // [ng] live groups, ascending
     int *n_live;
+    int *first;
 };
 
 template <int BUF_BYTES>
 __device__ __forceinline__ MaskBuf mask_buf(uint8_t *area, int b) {
     uint8_t *base = area + b * BUF_BYTES;
     return MaskBuf{reinterpret_cast<uint32_t *>(base), reinterpret_cast<int *>(base + kMaxKGroups * 16),
-                   reinterpret_cast<int *>(base + kMaxKGroups * 20)};
+                   reinterpret_cast<int *>(base + kMaxKGroups * 20),
+                   reinterpret_cast<int *>(base + kMaxKGroups * 20 + 4)};
+}
+
+// Decode lane masks (T <= 16 tokens in lanes 0..15 of the tile): lane i of the
+// warp takes group g0 + i, reads its mask byte for every token (one coalesced
+// 32-byte row segment per token) and forms the word of active tokens; lanes
+// 32..127 of the tile are always disabled.  Returns the number of live groups.
+__device__ __forceinline__ int build_decode_masks(const uint8_t *__restrict__ mask, int T, int ng,
+                                                  uint32_t *lanes, int *live) {
+    const int lane = threadIdx.x & 31;
+    int n_live = 0;
+    for (int g0 = 0; g0 < ng; g0 += 32) {
+        const int g = g0 + lane;
+        uint32_t word = 0;
+        if (g < ng) {
+            uint8_t v[16];
+#pragma unroll
+            for (int t = 0; t < 16; ++t) v[t] = t < T ? mask[static_cast<size_t>(t) * ng + g] : 0;
+#pragma unroll
+            for (int t = 0; t < 16; ++t) word |= (v[t] != 0 ? 1u : 0u) << t;
+            *reinterpret_cast<uint4 *>(lanes + g * 4) = make_uint4(~word, ~0u, ~0u, ~0u);
+        }
+        const uint32_t b = __ballot_sync(0xffffffffu, word != 0u);
+        if (word != 0u) live[n_live + __popc(b & ((1u << lane) - 1u))] = g;
+        n_live += __popc(b);
+    }
+    return n_live;
 }
 
 
@@ -88,14 +130,22 @@ __device__ __forceinline__ int build_tile_masks(const uint8_t *__restrict__ mask
         }
     };
     if ((ng & 15) == 0) {
-        for (int g0 = 0; g0 < ng; g0 += 16) {
-            uint4 v[Q];
+        // 16-byte loads of 16 groups; the loads of the next 16 groups are
+        // issued before the current ones are used.
+        auto load16 = [&](int g0, uint4 (&v)[Q]) {
 #pragma unroll
             for (int q = 0; q < Q; ++q) {
                 const int t = m0 + 32 * q + lane;
                 v[q] = t < T ? *reinterpret_cast<const uint4 *>(mask + static_cast<size_t>(t) * ng + g0)
                              : make_uint4(0, 0, 0, 0);
             }
+        };
+        uint4 v[Q];
+        load16(0, v);
+        for (int g0 = 0; g0 < ng; g0 += 16) {
+            uint4 nv[Q];
+            const bool more = g0 + 16 < ng;
+            if (more) load16(g0 + 16, nv);
 #pragma unroll
             for (int u = 0; u < 16; ++u) {
                 uint32_t w[Q];
@@ -105,6 +155,10 @@ __device__ __forceinline__ int build_tile_masks(const uint8_t *__restrict__ mask
                     w[q] = __ballot_sync(0xffffffffu, ((word >> ((u & 3) * 8)) & 0xFFu) != 0u);
                 }
                 emit(g0 + u, w);
+            }
+            if (more) {
+#pragma unroll
+                for (int q = 0; q < Q; ++q) v[q] = nv[q];
             }
         }
     } else {
@@ -132,11 +186,11 @@ __device__ __forceinline__ int build_tile_masks(const uint8_t *__restrict__ mask
     return n_live;
 }
 
-template <int BN>
+template <int BN, int AR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_k_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
                   const KArgs args) {
-    using C = KCfg<BN>;
+    using C = KCfg<BN, AR>;
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
@@ -158,8 +212,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ng = args.K / args.G;
     const int m_tiles = (T + BM - 1) / BM;
     const int n_tiles = args.N / BN;
-    const int n_items = m_tiles * n_tiles;
+    const int splits = AR == BM ? 1 : args.splits;
+    const int n_items = m_tiles * n_tiles * splits;
     const int kb_per_group = args.G / BK;
+    const bool partial_out = args.partial != nullptr;
+    const uint32_t stage_bytes = static_cast<uint32_t>(args.a_rows * BK * 2 + C::B_BYTES);
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < C::STAGES; ++s) {
@@ -189,7 +246,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
     // Accumulators start at zero: every MMA accumulates (lanes it skips must
-    // keep the value of the groups already added).
+    // keep the value of the groups already added).  Only the MMA issuer waits
+    // for the zeroing (named barrier 1: warps 1, 3..6); the producer and the
+    // mask builder start on the first tile at once.
     if (warp >= 3) {
         const int quad = warp & 3;
         uint32_t z[32];
@@ -199,24 +258,39 @@ __global__ void __launch_bounds__(kThreads, 1)
             tmem_st32(tmem_base + (static_cast<uint32_t>(quad * 32) << 16) + col, z);
         tmem_st_wait();
     }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
+    if (warp == 1 || warp >= 3) {
+        tc_fence_before();
+        named_barrier_sync(1, 5 * 32);
+        tc_fence_after();
+    }
 
     if (warp == 2) {
         // ===================== mask builder =====================
         int b = 0;
         uint32_t bphase = 0;
         for (int i = blockIdx.x; i < n_items && !*s_abort; i += gridDim.x) {
-            const int mt = i / n_tiles;
+            const int mt = i / (n_tiles * splits);
+            const int sp = (i - mt * n_tiles * splits) / n_tiles;
             const int m0 = mt * BM;
             int ok = 1;
             if (lane == 0) ok = mbar_wait(&mempty[b], bphase ^ 1u, args.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { *s_abort = 1; break; }
             const MaskBuf mbuf = mask_buf<C::MASK_BUF_BYTES>(mask_area, b);
-            const int n_live = build_tile_masks<4>(args.mask, T, ng, m0, mbuf.lanes, mbuf.live);
-            if (lane == 0) *mbuf.n_live = n_live;
+            int n_live, first = 0;
+            if constexpr (AR == BM) {
+                n_live = build_tile_masks<4>(args.mask, T, ng, m0, mbuf.lanes, mbuf.live);
+            } else {
+                // equal contiguous shares of the live groups, one per split
+                const int n_all = build_decode_masks(args.mask, T, ng, mbuf.lanes, mbuf.live);
+                const int per = (n_all + splits - 1) / splits;
+                first = min(n_all, sp * per);
+                n_live = min(n_all, first + per) - first;
+            }
+            if (lane == 0) {
+                *mbuf.n_live = n_live;
+                *mbuf.first = first;
+            }
             __threadfence_block();
             __syncwarp();
             if (lane == 0) mbar_arrive(&mfull[b]);  // release semantics publish the buffer
@@ -230,22 +304,24 @@ __global__ void __launch_bounds__(kThreads, 1)
         int b = 0;
         uint32_t bphase = 0;
         for (int i = blockIdx.x; i < n_items && !*s_abort; i += gridDim.x) {
-            const int mt = i / n_tiles, nt = i - mt * n_tiles;
+            const int mt = i / (n_tiles * splits);
+            const int nt = (i - mt * n_tiles * splits) % n_tiles;
             int ok = 1;
             if (lane == 0) ok = mbar_wait(&mfull[b], bphase, args.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { *s_abort = 1; break; }
             const MaskBuf mbuf = mask_buf<C::MASK_BUF_BYTES>(mask_area, b);
             const int n_live = *mbuf.n_live;
+            const int *live = mbuf.live + *mbuf.first;
             for (int li = 0; li < n_live && ok; ++li) {
-                const int g = mbuf.live[li];
+                const int g = live[li];
                 for (int kb = 0; kb < kb_per_group; ++kb) {
                     if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, args.status);
                     ok = __shfl_sync(0xffffffffu, ok, 0);
                     if (!ok) break;
                     if (lane == 0) {
                         uint8_t *sa = stages + stage * C::STAGE_BYTES;
-                        mbar_arrive_expect_tx(&full[stage], C::STAGE_BYTES);
+                        mbar_arrive_expect_tx(&full[stage], stage_bytes);
                         const int kx = g * args.G + kb * BK;
                         tma_load_2d(sa, &tmA, &full[stage], kx, mt * BM);
                         tma_load_2d(sa + C::A_BYTES, &tmB, &full[stage], kx, nt * BN);
@@ -280,9 +356,10 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const uint32_t d = tmem_base + static_cast<uint32_t>(acc * BN);
                 const MaskBuf mbuf = mask_buf<C::MASK_BUF_BYTES>(mask_area, b);
                 const int n_live = *mbuf.n_live;
+                const int *live = mbuf.live + *mbuf.first;
                 bool ok = true;
                 for (int li = 0; li < n_live && ok; ++li) {
-                    const int g = mbuf.live[li];
+                    const int g = live[li];
                     const uint32_t l0 = mbuf.lanes[g * 4 + 0], l1 = mbuf.lanes[g * 4 + 1];
                     const uint32_t l2 = mbuf.lanes[g * 4 + 2], l3 = mbuf.lanes[g * 4 + 3];
                     for (int kb = 0; kb < kb_per_group; ++kb) {
@@ -319,7 +396,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 32; ++q) z[q] = 0u;
         for (int i = blockIdx.x; i < n_items && !*s_abort; i += gridDim.x) {
-            const int mt = i / n_tiles, nt = i - mt * n_tiles;
+            const int mt = i / (n_tiles * splits);
+            const int rem = i - mt * n_tiles * splits;
+            const int sp = rem / n_tiles, nt = rem - sp * n_tiles;
             const int t = mt * BM + row;
             int ok = 1;
             if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, args.status);
@@ -335,7 +414,18 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(taddr + cb, yr);
                 tmem_ld_wait();
                 tmem_st32(taddr + cb, z);
-                if (t < T) {
+                if (partial_out) {
+                    // fp32 partial of this split; rows past T (and the lanes
+                    // the token box did not fill) were masked off and are not stored
+                    if (t < T) {
+                        float *pdst = args.partial + (static_cast<size_t>(sp) * T + t) * args.N + nt * BN + cb;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<float4 *>(pdst + 4 * q) =
+                                make_float4(__uint_as_float(yr[4 * q]), __uint_as_float(yr[4 * q + 1]),
+                                            __uint_as_float(yr[4 * q + 2]), __uint_as_float(yr[4 * q + 3]));
+                    }
+                } else if (t < T) {
 #pragma unroll
                     for (int q = 0; q < 4; ++q)
                         st_global_cs_v4(dst + cb + 8 * q,
@@ -361,15 +451,15 @@ __global__ void __launch_bounds__(kThreads, 1)
     }
 }
 
-template <int BN>
+template <int BN, int AR>
 cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a, int num_sms,
                      cudaStream_t s) {
-    using C = KCfg<BN>;
-    auto kern = gemm_k_kernel<BN>;
+    using C = KCfg<BN, AR>;
+    auto kern = gemm_k_kernel<BN, AR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int m_tiles = (a.T + BM - 1) / BM;
-    const int items = m_tiles * (a.N / BN);
+    const int items = m_tiles * (a.N / BN) * a.splits;
     const int grid = items < num_sms ? items : num_sms;
     kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(tmA, tmB, a);
     return cudaGetLastError();
@@ -380,12 +470,51 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs
 
 int gemm_k_max_groups() { return kMaxKGroups; }
 
+// Decode split count: each 128-column output tile becomes `splits` work items,
+// each holding an equal share of the tile's live groups.  The count minimises
+// the weight bytes of the busiest CTA (items dealt round-robin over the grid,
+// all groups taken as live) plus each SM's share of the fp32 partial traffic
+// (written here, read back by the finalize kernel); ties go to fewer splits.
+int gemm_k_decode_splits(int T, int K, int N, int G, int num_sms) {
+    const int ng = K / G;
+    const int n_tiles = N / 128;
+    double best = 0.0;
+    int best_s = 1;
+    for (int s = 1; s <= ng; ++s) {
+        const int g = (ng + s - 1) / s;
+        if ((ng + g - 1) / g != s) continue;  // same shares as a smaller split count
+        const long long items = static_cast<long long>(n_tiles) * s;
+        const long long waves = (items + num_sms - 1) / num_sms;
+        const double cta_bytes = static_cast<double>(waves) * g * G * 128 * 2;
+        const double partial = static_cast<double>(s) * T * N * 8 / num_sms;
+        const double cost = cta_bytes + partial;
+        if (s == 1 || cost < best) {
+            best = cost;
+            best_s = s;
+        }
+    }
+    return best_s;
+}
+
+size_t gemm_k_decode_workspace_bytes(int T, int K, int N, int G, int num_sms) {
+    return static_cast<size_t>(gemm_k_decode_splits(T, K, N, G, num_sms)) * T * N * sizeof(float);
+}
+
+cudaError_t launch_gemm_k_decode(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a0,
+                                 float *ws, int num_sms, cudaStream_t s) {
+    KArgs a = a0;
+    a.splits = gemm_k_decode_splits(a.T, a.K, a.N, a.G, num_sms);
+    a.partial = ws;
+    cudaError_t e = launch_t<128, 16>(tmA, tmB, a, num_sms, s);
+    if (e != cudaSuccess) return e;
+    return launch_decode_k_finalize(ws, a.splits, a.T * a.N, a.out, s);
+}
 
 cudaError_t launch_gemm_k(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a,
                           int num_sms, cudaStream_t s) {
-    if (bn == 256) return launch_t<256>(tmA, tmB, a, num_sms, s);
-    if (bn == 128) return launch_t<128>(tmA, tmB, a, num_sms, s);
-    if (bn == 64) return launch_t<64>(tmA, tmB, a, num_sms, s);
+    if (bn == 256) return launch_t<256, BM>(tmA, tmB, a, num_sms, s);
+    if (bn == 128) return launch_t<128, BM>(tmA, tmB, a, num_sms, s);
+    if (bn == 64) return launch_t<64, BM>(tmA, tmB, a, num_sms, s);
     return cudaErrorInvalidValue;
 }
 

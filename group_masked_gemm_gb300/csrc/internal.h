@@ -23,9 +23,14 @@ struct MNArgs {
 
 struct KArgs {
     const uint8_t *mask;  // [T, n_groups]
-    uint16_t *out;        // bf16 [T, N]
+    uint16_t *out;        // bf16 [T, N] (when partial == nullptr)
     int T, K, N, G;
     int *status;
+    // Decode only: item (n-tile, split s) reduces the s-th equal share of the
+    // live groups and writes fp32 partial[s][T][N].
+    float *partial = nullptr;
+    int splits = 1;
+    int a_rows = 128;  // rows of the token-row TMA box (<= 128)
 };
 
 struct DecodeArgs {
@@ -52,6 +57,14 @@ cudaError_t launch_gemm_mn(MNMode mode, int bn, const CUtensorMap &tmB0, const C
 cudaError_t launch_gemm_k(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
                           const KArgs &a, int num_sms, cudaStream_t s);
 
+// Decode (T <= 16) GEMM-K on the GEMM-K kernel with the groups split over
+// CTAs: tmA box 64 x min(T,16) (a.a_rows), tmB box 64 x 128, N % 128 == 0;
+// ws: gemm_k_decode_workspace_bytes(T, K, N, G, num_sms) of fp32 partials.
+int gemm_k_decode_splits(int T, int K, int N, int G, int num_sms);
+size_t gemm_k_decode_workspace_bytes(int T, int K, int N, int G, int num_sms);
+cudaError_t launch_gemm_k_decode(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a,
+                                 float *ws, int num_sms, cudaStream_t s);
+
 cudaError_t launch_decode_mn(MNMode mode, const DecodeArgs &a, int num_sms, cudaStream_t s);
 // ws: fp32 partial sums, decode_k_workspace_bytes(T, K, N, G) bytes.
 cudaError_t launch_decode_k(const DecodeArgs &a, float *ws, cudaStream_t s);
@@ -65,11 +78,8 @@ cudaError_t launch_decode_k_finalize(const float *ws, int splits, int TN, uint16
 // [T, K], box 64 x min(T, 16).  GEMM-K: tmW box 64 x 128 (N % 128 == 0),
 // tmA: the token rows [T, K], box 64 x min(T, 16).
 int decode_tc_rows_per_item();
-size_t decode_tc_k_workspace_bytes(int T, int K, int N, int G);
 cudaError_t launch_decode_mn_tc(MNMode mode, const CUtensorMap &tmW0, const CUtensorMap &tmW1,
                                 const CUtensorMap &tmX, const DecodeArgs &a, int *status,
                                 int num_sms, cudaStream_t s);
-cudaError_t launch_decode_k_tc(const CUtensorMap &tmW, const CUtensorMap &tmA, const DecodeArgs &a,
-                               float *ws, int *status, cudaStream_t s);
 
 }  // namespace wide

@@ -91,7 +91,9 @@ def test_proj_mn_parity(T, K, N, G, keep):
 @pytest.mark.parametrize("T,K,N,G,keep", [
     (64, 1024, 256, 128, 0.5), (300, 1024, 256, 64, 0.5), (300, 2048, 320, 128, 0.5),
     (517, 2048, 384, 256, 0.4), (517, 2048, 256, 512, 0.6), (200, 1024, 512, 128, 1.0),
-    (200, 1024, 512, 128, 0.0), (1000, 1536, 256, 128, 0.08)])
+    (200, 1024, 512, 128, 0.0), (1000, 1536, 256, 128, 0.08),
+    # G = 512 (o_proj-sized groups), ragged T, all-active and all-inactive
+    (300, 2048, 512, 512, 1.0), (300, 2048, 512, 512, 0.0), (1029, 4096, 768, 512, 0.34)])
 def test_gemm_k_parity(T, K, N, G, keep):
     rng = np.random.default_rng(T * 3 + G)
     A = _bits_dev(rng, (T, K))
@@ -177,6 +179,44 @@ def test_decode_ragged_and_empty():
     ops.device_status()
     assert_close(to_f64(Y), oracle.proj_mn(X, W, mask, G), "decode proj_mn")
     assert (to_f64(Z)[2] == 0).all()
+
+
+@pytest.mark.parametrize("T,K,N,G,keep", [
+    (2, 2560, 384, 64, 0.5),      # 40 groups (not a multiple of 32), 3 output tiles
+    (7, 4096, 1024, 512, 0.3),    # ragged token box, o_proj-sized groups
+    (13, 1536, 256, 128, 1.0),    # every group live
+    (16, 2048, 512, 256, 0.0),    # no group live: every split writes zeros
+    (1, 14336, 4096, 128, 0.05),  # fewer live groups than splits
+])
+def test_decode_k_split_edges(T, K, N, G, keep):
+    """Decode GEMM-K: live groups dealt in equal shares over the splits, fp32
+    partials summed in split order."""
+    rng = np.random.default_rng(T * 7 + K)
+    A = _bits_dev(rng, (T, K))
+    W = _bits_dev(rng, (N, K), 0.02)
+    mask = (rng.random((T, K // G)) < keep).astype(np.uint8)
+    Y = _nan_like((T, N))
+    ops.proj_k(to_dev(A), to_dev(W), mask_dev(mask), None, None, G, out=Y)
+    Y2 = _nan_like((T, N))
+    ops.proj_k(to_dev(A), to_dev(W), mask_dev(mask), None, None, G, out=Y2)
+    ops.device_status()
+    assert torch.equal(Y, Y2)  # deterministic
+    assert_close(to_f64(Y), oracle.proj_k(A, W, mask, G), "decode proj_k")
+
+
+@pytest.mark.parametrize("T,K,N,G", [(5, 4096, 1024, 128), (8, 2048, 768, 256)])
+def test_decode_mn_tensor_core_sizes(T, K, N, G):
+    """Decode GEMM-MN above 4 tokens (tensor-core kernel), plain and gate/up."""
+    rng = np.random.default_rng(T + N)
+    X = _bits_dev(rng, (T, K))
+    W = _bits_dev(rng, (N, K), 0.02)
+    W2 = _bits_dev(rng, (N, K), 0.02)
+    mask = (rng.random((T, N // G)) < 0.5).astype(np.uint8)
+    Y = ops.proj_mn(to_dev(X), to_dev(W), mask_dev(mask), None, None, G)
+    H = ops.gemm_mn_gate_up(to_dev(X), to_dev(W), to_dev(W2), mask_dev(mask), None, None, G)
+    ops.device_status()
+    assert_close(to_f64(Y), oracle.proj_mn(X, W, mask, G), "decode proj_mn")
+    assert_close(to_f64(H), oracle.gate_up(X, W, W2, mask, G), "decode gate_up")
 
 
 # ------------------------------------------------ determinism and CUDA graphs ---
