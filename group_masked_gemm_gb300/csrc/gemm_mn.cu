@@ -295,20 +295,28 @@ __global__ void __launch_bounds__(kThreads, 1)
         // cp.async arrive, so no thread waits for its own copies; the MMA
         // thread makes them visible to the tensor core (proxy fence) after
         // acquiring the barrier.
+        // The token indices of the next tile are loaded while the current
+        // tile streams, so no tile starts with a dependent global load.
         const int gw = warp - 6;
         const int sub = lane >> 3, chunk = lane & 7;
-        int stage = 0;
-        uint32_t phase = 0;
-        for (int i = blockIdx.x; i < sch.n_total && !*s_abort; i += gridDim.x) {
+        auto row_token = [&](int i) -> int {  // this lane's row of compute item i, or -1
             const Item it = decode_item(sch, i);
-            if (it.zero) continue;
-            const int32_t *pg = args.perm + static_cast<size_t>(it.g) * T;
             const int rows_valid = min(BM, sch.counts[it.g] - it.m * BM);
             const int my_row = 32 * gw + lane;
-            const int my_tok = my_row < rows_valid ? ld_nc_s32(pg + it.m * BM + my_row) : -1;
+            return my_row < rows_valid
+                       ? ld_nc_s32(args.perm + static_cast<size_t>(it.g) * T + it.m * BM + my_row)
+                       : -1;
+        };
+        int stage = 0;
+        uint32_t phase = 0;
+        // compute items are exactly i < n_compute (the zero-fill items follow them)
+        int next_tok = blockIdx.x < sch.n_compute ? row_token(blockIdx.x) : -1;
+        for (int i = blockIdx.x; i < sch.n_compute && !*s_abort; i += gridDim.x) {
+            const int my_tok = next_tok;
             int toks[8];
 #pragma unroll
             for (int q = 0; q < 8; ++q) toks[q] = __shfl_sync(0xffffffffu, my_tok, 4 * q + sub);
+            if (i + static_cast<int>(gridDim.x) < sch.n_compute) next_tok = row_token(i + gridDim.x);
             for (int kb = 0; kb < k_blocks; ++kb) {
                 int ok = 1;
                 if (lane == 0) ok = mbar_wait(&empty[stage], phase ^ 1u, args.status);
