@@ -342,18 +342,36 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int row = quad * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
-        for (int i = blockIdx.x; i < sch.n_total && !*s_abort; i += gridDim.x) {
-            const Item it = decode_item(sch, i);
+        // This CTA's items are i = blockIdx.x + k * gridDim.x: compute items
+        // first (i < n_compute), then zero-fill items.  Zero-fill items need
+        // only stores, so they are spread between the compute tiles'
+        // epilogues, while the tensor core works on the next tile, instead of
+        // being written after the last MMA.
+        const int bx = static_cast<int>(blockIdx.x), grid = static_cast<int>(gridDim.x);
+        const int n_comp_mine = sch.n_compute > bx ? (sch.n_compute - bx + grid - 1) / grid : 0;
+        const int n_all_mine = sch.n_total > bx ? (sch.n_total - bx + grid - 1) / grid : 0;
+        const int n_zero_mine = n_all_mine - n_comp_mine;
+        const int zero_per_tile = n_comp_mine > 0 ? (n_zero_mine + n_comp_mine - 1) / n_comp_mine : n_zero_mine;
+        int zk = 0;  // zero-fill items written so far
+        auto write_zero_items = [&](int count) {
+            for (int c = 0; c < count && zk < n_zero_mine; ++c, ++zk) {
+                const Item it = decode_item(sch, bx + (n_comp_mine + zk) * grid);
+                const int j = it.m * BM + row;
+                if (j < T) {
+                    const int token = ld_nc_s32(args.perm + static_cast<size_t>(it.g) * T + j);
+                    uint16_t *orow = args.out + static_cast<size_t>(token) * args.n_out + it.g * args.G;
+                    for (int cidx = 0; cidx < args.G; cidx += 8) st_global_cs_v4(orow + cidx, 0, 0, 0, 0);
+                }
+            }
+        };
+        for (int k = 0; k < n_comp_mine && !*s_abort; ++k) {
+            write_zero_items(zero_per_tile);
+            const Item it = decode_item(sch, bx + k * grid);
             const int32_t *pg = args.perm + static_cast<size_t>(it.g) * T;
             const int j = it.m * BM + row;
             const bool valid = j < T;
             const int token = valid ? ld_nc_s32(pg + j) : 0;
             uint16_t *orow = args.out + static_cast<size_t>(token) * args.n_out + it.g * args.G;
-            if (it.zero) {
-                if (valid)
-                    for (int cidx = 0; cidx < args.G; cidx += 8) st_global_cs_v4(orow + cidx, 0, 0, 0, 0);
-                continue;
-            }
             const bool active = j < sch.counts[it.g];
             int ok = 1;
             if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, args.status);
@@ -396,6 +414,7 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (lane == 0) mbar_arrive(&tempty[acc]);
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
         }
+        if (!*s_abort) write_zero_items(n_zero_mine);
     }
 
     tc_fence_before();
