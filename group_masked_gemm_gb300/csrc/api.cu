@@ -37,6 +37,10 @@ bool good_ptr(const void *p) { return p != nullptr && aligned16(p); }
 
 bool good_group(int G) { return G == 64 || G == 128 || G == 256 || G == 512; }
 
+// The M-axis (dynamic depth) case: one group spanning the whole grouped
+// dimension (n_groups = 1, App. B "Implementation of GEMM-MN"), tile-aligned.
+bool whole_width_group(int G, int width) { return G == width && G % 256 == 0; }
+
 // Group sizes come from the tile-size set {2^k : k >= 4} (Sec. 3.1); members
 // of the set outside {64..512} are valid but not implemented.
 wide_status_t bad_group_status(int G) {
@@ -117,7 +121,7 @@ wide_status_t check_mn(const void *X, const void *W0, const void *W1, const void
         !good_ptr(out))
         return WIDE_ERR_INVALID_ARG;
     if (T < 1 || K < 64 || N < 64 || K % 64 || N % 64) return WIDE_ERR_INVALID_ARG;
-    if (!good_group(G)) return bad_group_status(G);
+    if (!good_group(G) && !whole_width_group(G, N)) return bad_group_status(G);
     if (N % G) return WIDE_ERR_INVALID_ARG;
     if (N / G > wide::kMaxGroups) return WIDE_ERR_UNSUPPORTED;
     if (T > kDecodeMaxT && (!good_ptr(perm) || !good_ptr(counts))) return WIDE_ERR_INVALID_ARG;
@@ -131,7 +135,7 @@ wide_status_t check_k(const void *A, const void *W, const void *mask, int T, int
     if (!good_ptr(A) || !good_ptr(W) || !good_ptr(mask) || !good_ptr(out))
         return WIDE_ERR_INVALID_ARG;
     if (T < 1 || K < 64 || N < 64 || K % 64 || N % 64) return WIDE_ERR_INVALID_ARG;
-    if (!good_group(G)) return bad_group_status(G);
+    if (!good_group(G) && !whole_width_group(G, K)) return bad_group_status(G);
     if (K % G) return WIDE_ERR_INVALID_ARG;
     if (K / G > wide::gemm_k_max_groups()) return WIDE_ERR_UNSUPPORTED;
     const size_t need = wide_gemm_k_workspace_size(T, K, N, G);
@@ -194,6 +198,8 @@ wide_status_t run_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask, i
             wide::launch_gemm_k_decode(tmA, tmB, a, static_cast<float *>(ws), ctx.num_sms, s));
     }
     if (T <= kDecodeMaxT) {
+        // a single group wider than the staged slice (whole-width G) does not fit
+        if (wide::decode_k_smem_bytes(T, K, G) > 200 * 1024) return WIDE_ERR_UNSUPPORTED;
         wide::DecodeArgs a{A, W, nullptr, mask, out, T, K, N, G};
         return from_cuda(wide::launch_decode_k(a, static_cast<float *>(ws), s));
     }

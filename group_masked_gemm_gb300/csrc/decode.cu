@@ -263,6 +263,11 @@ int decode_k_groups_per_split(int T, int K, int G) {
     return (ng + splits - 1) / splits;  // equal splits on group boundaries
 }
 
+size_t decode_k_smem_bytes(int T, int K, int G) {
+    const int gps = decode_k_groups_per_split(T, K, G);
+    return static_cast<size_t>(tm_of(T)) * gps * G * 2 + static_cast<size_t>(gps) * 4;
+}
+
 size_t decode_k_workspace_bytes(int T, int K, int N, int G) {
     const int ng = K / G;
     const int gps = decode_k_groups_per_split(T, K, G);

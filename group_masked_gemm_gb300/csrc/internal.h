@@ -66,7 +66,9 @@ cudaError_t launch_gemm_k_decode(const CUtensorMap &tmA, const CUtensorMap &tmB,
                                  float *ws, int num_sms, cudaStream_t s);
 
 cudaError_t launch_decode_mn(MNMode mode, const DecodeArgs &a, int num_sms, cudaStream_t s);
-// ws: fp32 partial sums, decode_k_workspace_bytes(T, K, N, G) bytes.
+// ws: fp32 partial sums, decode_k_workspace_bytes(T, K, N, G) bytes; the
+// kernel stages decode_k_smem_bytes(T, K, G) of shared memory.
+size_t decode_k_smem_bytes(int T, int K, int G);
 cudaError_t launch_decode_k(const DecodeArgs &a, float *ws, cudaStream_t s);
 size_t decode_k_workspace_bytes(int T, int K, int N, int G);
 size_t decode_mn_smem_bytes(int T, int K, int n_groups);

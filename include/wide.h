@@ -19,7 +19,10 @@
  *     enqueue work on it: no host synchronisation, no device-to-host copy, no
  *     allocation.  Nothing is returned to the host through memory.
  *   - Shapes: T >= 1; G in {64, 128, 256, 512}; every feature dimension is a
- *     multiple of 64 and of G where it is grouped.
+ *     multiple of 64 and of G where it is grouped.  G may also equal the whole
+ *     grouped dimension (N for GEMM-MN, K for GEMM-K) when that is a multiple
+ *     of 256: one group per token, the M-axis (dynamic depth) special case
+ *     N_G = 1 of App. B ("Implementation of GEMM-MN"); the mask is [T, 1].
  *   - Outputs are fully overwritten (never accumulated into): MN outputs hold
  *     exact zeros in inactive (token, group) blocks; K outputs of a token with
  *     no active group are zero.  K calls ignore the values of A inside

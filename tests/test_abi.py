@@ -77,6 +77,14 @@ def test_argument_errors_are_reported_before_any_launch(libwide):
     assert L.wide_gemm_k_down(good, good, good, good, good, 64, 1024, 250, 128, good,
                               None, 0, None) == 1            # d_model not a multiple of 64
     assert L.wide_proj_mn(good, good, good, good, good, 64, 4096, 4096, 96, good, None) == 1
+    # one group spanning the whole grouped dimension (N_G = 1) passes validation
+    # when it is a multiple of 256; with no GPU here the call then fails at launch
+    assert L.wide_proj_mn(good, good, good, good, good, 64, 4096, 1536, 1536, good, None) == 4
+    assert L.wide_proj_mn(good, good, good, good, good, 64, 4096, 640, 640, good, None) == 1
+    assert L.wide_gemm_k_down(good, good, good, good, good, 64, 2048, 256, 2048, good,
+                              None, 0, None) == 4
+    assert L.wide_gemm_k_down(good, good, good, good, good, 64, 2048, 256, 1024, good,
+                              None, 0, None) == 2            # G = 1024 < K = 2048: tile size, not implemented
 
 
 def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):

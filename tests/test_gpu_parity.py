@@ -146,6 +146,59 @@ def test_tiny_config_ffn():
     assert_close(to_f64(Y), oracle.ffn(inp.X, inp.Wg, inp.Wu, inp.Wd, inp.mask, inp.G), "tiny")
 
 
+# ------------------------------------------- M-axis depth (n_groups = 1) ---
+
+@pytest.mark.parametrize("T,K,N,keep", [(300, 512, 768, 0.5), (129, 256, 1024, 0.7), (7, 1024, 512, 0.5),
+                                        (2, 768, 256, 1.0), (40, 512, 1536, 0.0)])
+def test_whole_width_group_mn(T, K, N, keep):
+    """G = N: each token runs the whole projection or nothing (App. B, N_G = 1)."""
+    rng = np.random.default_rng(T + N)
+    X = _bits_dev(rng, (T, K))
+    W = _bits_dev(rng, (N, K), 0.02)
+    W2 = _bits_dev(rng, (N, K), 0.02)
+    mask = (rng.random((T, 1)) < keep).astype(np.uint8)
+    m = mask_dev(mask)
+    perm, counts = ops.reorder_masks(m)
+    Y = _nan_like((T, N))
+    ops.proj_mn(to_dev(X), to_dev(W), m, perm, counts, N, out=Y)
+    H = _nan_like((T, N))
+    ops.gemm_mn_gate_up(to_dev(X), to_dev(W), to_dev(W2), m, perm, counts, N, out=H)
+    ops.device_status()
+    Yg, Hg = to_f64(Y), to_f64(H)
+    assert not np.isnan(Yg).any() and not np.isnan(Hg).any()
+    assert (Yg[mask[:, 0] == 0] == 0).all() and (Hg[mask[:, 0] == 0] == 0).all()
+    assert_close(Yg, oracle.proj_mn(X, W, mask, N), "proj_mn G=N")
+    assert_close(Hg, oracle.gate_up(X, W, W2, mask, N), "gate_up G=N")
+
+
+@pytest.mark.parametrize("T,K,N,keep", [(300, 768, 384, 0.5), (1029, 1024, 256, 0.3), (5, 1536, 512, 0.6),
+                                        (16, 512, 320, 0.5)])
+def test_whole_width_group_k(T, K, N, keep):
+    """G = K: each token's whole reduction is kept or dropped."""
+    rng = np.random.default_rng(T + K)
+    A = _bits_dev(rng, (T, K))
+    W = _bits_dev(rng, (N, K), 0.02)
+    mask = (rng.random((T, 1)) < keep).astype(np.uint8)
+    m = mask_dev(mask)
+    perm, counts = ops.reorder_masks(m)
+    Y = _nan_like((T, N))
+    ops.proj_k(to_dev(A), to_dev(W), m, perm, counts, K, out=Y)
+    ops.device_status()
+    Yg = to_f64(Y)
+    assert not np.isnan(Yg).any()
+    assert (Yg[mask[:, 0] == 0] == 0).all()
+    assert_close(Yg, oracle.proj_k(A, W, mask, K), "proj_k G=K")
+
+
+def test_whole_width_group_ffn():
+    """The whole FFN with one group per token (dynamic depth on the FFN)."""
+    inp = syn.ffn_inputs(500, 256, 1024, 1024, seed=11, keep=0.5)
+    Y = ops.ffn_forward(to_dev(inp.X), to_dev(inp.Wg), to_dev(inp.Wu), to_dev(inp.Wd),
+                        mask_dev(inp.mask), inp.G)
+    ops.device_status()
+    assert_close(to_f64(Y), oracle.ffn(inp.X, inp.Wg, inp.Wu, inp.Wd, inp.mask, inp.G), "ffn G=F")
+
+
 # ------------------------------------------------------------------- decode ---
 
 @pytest.mark.parametrize("T", [1, 4, 16])

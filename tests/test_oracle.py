@@ -204,6 +204,24 @@ def test_single_group_mask_is_dense_slice(tiny):
     np.testing.assert_allclose(Y, y_ref, rtol=1e-10, atol=1e-12)
 
 
+def test_whole_width_group_is_token_mask_times_dense(tiny):
+    """N_G = 1 (App. B: M-axis depth is the one-group case of GEMM-MN/GEMM-K):
+    every token either gets the whole dense row or zero."""
+    rng = np.random.default_rng(5)
+    T = tiny.T
+    m = (rng.random((T, 1)) < 0.5).astype(np.uint8)
+    X, Wg, Wu, Wd = (_f64(a) for a in (tiny.X, tiny.Wg, tiny.Wu, tiny.Wd))
+    keep = m[:, :1].astype(np.float64)
+    np.testing.assert_allclose(oracle.proj_mn(tiny.X, tiny.Wg, m, tiny.F), keep * (X @ Wg.T),
+                               rtol=1e-10, atol=1e-12)
+    np.testing.assert_allclose(oracle.proj_k(tiny.X, tiny.Wg, m, tiny.D), keep * (X @ Wg.T),
+                               rtol=1e-10, atol=1e-12)
+    a = X @ Wg.T
+    y = keep * ((a * expit(a) * (X @ Wu.T)) @ Wd.T)
+    np.testing.assert_allclose(oracle.ffn(tiny.X, tiny.Wg, tiny.Wu, tiny.Wd, m, tiny.F), y,
+                               rtol=1e-10, atol=1e-12)
+
+
 # --- invariants ---------------------------------------------------------------------
 
 def test_complement_linearity(tiny):
