@@ -10,6 +10,7 @@ header for the passages of "WIDE: Boosting Adaptive LLM Inference via
 Token-level Dynamic Width Pruning" each function restates.
 """
 from .oracle import (  # noqa: F401
+    router,
     build,
     library_path,
     reorder,

@@ -56,6 +56,8 @@ def _load():
         lib.oracle_gate_up.restype = None
         lib.oracle_ffn.argtypes = [p, p, p, p, p, i, i, i, i, p, i, p, p]
         lib.oracle_ffn.restype = None
+        lib.oracle_router.argtypes = [p, p, p, i, i, i, i, p, p]
+        lib.oracle_router.restype = None
         _lib = lib
     return _lib
 
@@ -163,3 +165,21 @@ def ffn(X, Wg, Wu, Wd, mask, G, rows=None):
                        T, D, F, G, None if r is None else _ptr(r), R,
                        _ptr(Y), _ptr(scratch))
     return Y
+
+
+def router(X, W1, W2):
+    """Eq. 4-5: logits R [T, 2*n_groups] (column 2g+c) and mask [T, n_groups].
+
+    X bf16 [T, D], W1 bf16 [r, D], W2 bf16 [2*n_groups, r] (as bit patterns).
+    mask[t,g] = R[t,g,0] >= R[t,g,1] with the logits rounded to float."""
+    X = _c(X, np.uint16)
+    W1 = _c(W1, np.uint16)
+    W2 = _c(W2, np.uint16)
+    T, D = X.shape
+    r = W1.shape[0]
+    assert W1.shape == (r, D) and W2.shape[1] == r and W2.shape[0] % 2 == 0 and r <= 1024
+    ng = W2.shape[0] // 2
+    logits = np.empty((T, 2 * ng), np.float64)
+    mask = np.empty((T, ng), np.uint8)
+    _load().oracle_router(_ptr(X), _ptr(W1), _ptr(W2), T, D, r, ng, _ptr(logits), _ptr(mask))
+    return logits, mask

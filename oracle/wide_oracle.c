@@ -17,6 +17,9 @@
  *     o_proj on in-features), G = (Hq/Hk) d.
  *   - App. B, "Implementation of GEMM-K", Eq. 21:
  *     C[m,n] = sum_g M[m,g] sum_{k in K_g} A[m,k] B[n,k].
+ *   - Sec. 3.1 "Routing Components", Eq. 4-5: bottleneck router
+ *     R = reshape(X W1 W2) in R^{T x N_G x 2}, inference mask
+ *     M = 1[argmax_c R[...,c] = 0] (class 0 executes, class 1 skips).
  *
  * Arithmetic: every bf16 input is decoded exactly to double and every sum
  * is accumulated in double (the pages fix no precision; double makes the
@@ -30,7 +33,13 @@
  *     in ascending original row index; I is a full permutation.
  *   - A mask byte != 0 means "active".
  *   - Channel f belongs to group floor(f / G) (contiguous groups, Sec. 3.1).
- *   - Weights are stored [out_features, in_features] (B in R^{N x K}, Sec. 3.3).
+ *   - Weights are stored [out_features, in_features] (B in R^{N x K}, Sec. 3.3);
+ *     the router's W1 (D x r on the page) is stored [r, D] and W2 (r x 2N_G)
+ *     is stored [2N_G, r].
+ *   - The reshape of the 2N_G router outputs to (N_G, 2) is row-major: output
+ *     column 2g + c is class c of group g.
+ *   - argmax over the two classes returns the first maximum, so a tie
+ *     (R[t,g,0] == R[t,g,1]) selects class 0: the group executes.
  */
 #include <math.h>
 #include <stddef.h>
@@ -192,6 +201,43 @@ void oracle_ffn(const uint16_t *X, const uint16_t *Wg, const uint16_t *Wu,
                          bf16_to_double(Wd[(size_t)n * F + f]);
             }
             Y[(size_t)i * D + n] = y;
+        }
+    }
+}
+
+/*
+ * Router of Sec. 3.1 (Eq. 4) and its inference mask (Eq. 5):
+ *   z[t, j]    = sum_d X[t,d] W1[j,d]                 (j < r)
+ *   R[t, g, c] = sum_j z[t,j] W2[2g+c, j]             (c in {0, 1})
+ *   mask[t, g] = 1 if argmax_c R[t,g,c] == 0, i.e. R[t,g,0] >= R[t,g,1]
+ *   X : bf16 [T, D];  W1 : bf16 [r, D];  W2 : bf16 [2*n_groups, r]
+ *   logits : double [T, 2*n_groups] (R, column 2g + c);  mask : uint8 [T, n_groups]
+ *   The decision is taken on the logits rounded to float, the precision the
+ *   GPU kernel decides in; logits are returned unrounded.
+ */
+void oracle_router(const uint16_t *X, const uint16_t *W1, const uint16_t *W2,
+                   int T, int D, int r, int n_groups, double *logits, uint8_t *mask)
+{
+    const int nc = 2 * n_groups;
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int t = 0; t < T; ++t) {
+        double z[1024];
+        for (int j = 0; j < r; ++j) {
+            double acc = 0.0;
+            for (int d = 0; d < D; ++d)
+                acc += bf16_to_double(X[(size_t)t * D + d]) * bf16_to_double(W1[(size_t)j * D + d]);
+            z[j] = acc;
+        }
+        for (int c = 0; c < nc; ++c) {
+            double acc = 0.0;
+            for (int j = 0; j < r; ++j)
+                acc += z[j] * bf16_to_double(W2[(size_t)c * r + j]);
+            logits[(size_t)t * nc + c] = acc;
+        }
+        for (int g = 0; g < n_groups; ++g) {
+            const float r0 = (float)logits[(size_t)t * nc + 2 * g];
+            const float r1 = (float)logits[(size_t)t * nc + 2 * g + 1];
+            mask[(size_t)t * n_groups + g] = (uint8_t)(r0 >= r1 ? 1 : 0);
         }
     }
 }

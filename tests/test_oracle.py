@@ -222,6 +222,60 @@ def test_whole_width_group_is_token_mask_times_dense(tiny):
                                rtol=1e-10, atol=1e-12)
 
 
+def test_router_golden_eq4_5():
+    with open(os.path.join(GOLDEN, "router_eq4_5_example.json")) as f:
+        gold = json.load(f)
+    X, W1, W2 = (syn.bf16_bits(np.array(gold[k], np.float32)) for k in ("X", "W1", "W2"))
+    logits, mask = oracle.router(X, W1, W2)
+    np.testing.assert_array_equal(logits, np.array(gold["logits"], np.float64))
+    np.testing.assert_array_equal(mask, np.array(gold["mask"], np.uint8))
+
+
+def _router_inputs(seed, T=96, D=192, r=16, ng=12):
+    rng = np.random.default_rng(seed)
+    X = syn.bf16_bits(rng.standard_normal((T, D), dtype=np.float32))
+    W1 = syn.bf16_bits(rng.standard_normal((r, D), dtype=np.float32) * np.float32(D ** -0.5))
+    W2 = syn.bf16_bits(rng.standard_normal((2 * ng, r), dtype=np.float32) * np.float32(r ** -0.5))
+    return X, W1, W2
+
+
+def test_router_class_swap_complements_mask():
+    """Swapping the two class rows of every group exchanges R0 and R1, so the
+    mask flips everywhere except at exact ties (which stay active)."""
+    X, W1, W2 = _router_inputs(21)
+    logits, mask = oracle.router(X, W1, W2)
+    W2s = W2.reshape(-1, 2, W2.shape[1])[:, ::-1, :].reshape(W2.shape).copy()
+    logits_s, mask_s = oracle.router(X, W1, W2s)
+    np.testing.assert_array_equal(logits_s.reshape(len(X), -1, 2), logits.reshape(len(X), -1, 2)[:, :, ::-1])
+    tie = logits[:, 0::2].astype(np.float32) == logits[:, 1::2].astype(np.float32)
+    np.testing.assert_array_equal(mask_s[~tie], 1 - mask[~tie])
+    assert 0.2 < mask.mean() < 0.8   # random router weights keep about half
+
+
+def test_router_scale_invariance_and_ties():
+    """Doubling X (exact in bf16) doubles every logit and keeps every decision;
+    identical class rows give exact ties, which execute (class 0)."""
+    X, W1, W2 = _router_inputs(22)
+    logits, mask = oracle.router(X, W1, W2)
+    X2 = syn.bf16_bits(2.0 * syn.bf16_to_f32(X))
+    logits2, mask2 = oracle.router(X2, W1, W2)
+    np.testing.assert_array_equal(logits2, 2.0 * logits)
+    np.testing.assert_array_equal(mask2, mask)
+    W2t = W2.copy()
+    W2t[1::2] = W2t[0::2]
+    _, mask_t = oracle.router(X, W1, W2t)
+    assert mask_t.all()
+
+
+def test_router_tokens_are_independent():
+    X, W1, W2 = _router_inputs(23)
+    order = np.random.default_rng(1).permutation(len(X))
+    logits, mask = oracle.router(X, W1, W2)
+    logits_p, mask_p = oracle.router(X[order].copy(), W1, W2)
+    np.testing.assert_array_equal(logits_p, logits[order])
+    np.testing.assert_array_equal(mask_p, mask[order])
+
+
 # --- invariants ---------------------------------------------------------------------
 
 def test_complement_linearity(tiny):
