@@ -251,6 +251,34 @@ wide_status_t wide_reorder_masks(const uint8_t *mask, int T, int n_groups, int32
                                           static_cast<cudaStream_t>(stream)));
 }
 
+wide_status_t wide_router_masks(const uint16_t *X, const uint16_t *W1, const uint16_t *W2, int T,
+                                int d_model, int r, int n_groups, uint8_t *mask, float *logits,
+                                void *stream) {
+    if (!good_ptr(X) || !good_ptr(W1) || !good_ptr(W2) || !good_ptr(mask)) return WIDE_ERR_INVALID_ARG;
+    if (logits != nullptr && !aligned16(logits)) return WIDE_ERR_INVALID_ARG;
+    if (T < 1 || d_model < 64 || d_model % 64 || r < 16 || r % 16 || n_groups < 1)
+        return WIDE_ERR_INVALID_ARG;
+    if (!wide::router_supported(r, n_groups)) return WIDE_ERR_UNSUPPORTED;
+    DeviceCtx ctx;
+    wide_status_t st = device_ctx(&ctx);
+    if (st != WIDE_OK) return st;
+    CUtensorMap tmX, tmW1;
+    if ((st = encode_bf16_2d(&tmX, X, T, d_model, 128)) != WIDE_OK) return st;
+    if ((st = encode_bf16_2d(&tmW1, W1, r, d_model, r)) != WIDE_OK) return st;
+    wide::RouterArgs a{W2, mask, logits, T, d_model, r, n_groups, ctx.status};
+    return from_cuda(wide::launch_router(tmX, tmW1, a, ctx.num_sms, static_cast<cudaStream_t>(stream)));
+}
+
+wide_status_t wide_route_and_reorder(const uint16_t *X, const uint16_t *W1, const uint16_t *W2,
+                                     int T, int d_model, int r, int n_groups, uint8_t *mask,
+                                     int32_t *perm, int32_t *counts, void *ws, size_t ws_bytes,
+                                     void *stream) {
+    if (!good_ptr(perm) || !good_ptr(counts) || n_groups > 65535) return WIDE_ERR_INVALID_ARG;
+    wide_status_t st = wide_router_masks(X, W1, W2, T, d_model, r, n_groups, mask, nullptr, stream);
+    if (st != WIDE_OK) return st;
+    return wide_reorder_masks(mask, T, n_groups, perm, counts, ws, ws_bytes, stream);
+}
+
 wide_status_t wide_gemm_mn_gate_up(const uint16_t *X, const uint16_t *W_gate,
                                    const uint16_t *W_up, const uint8_t *mask,
                                    const int32_t *perm, const int32_t *counts, int T, int d_model,

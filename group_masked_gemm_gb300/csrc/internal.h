@@ -33,6 +33,15 @@ struct KArgs {
     int a_rows = 128;  // rows of the token-row TMA box (<= 128)
 };
 
+struct RouterArgs {
+    const uint16_t *W2;  // bf16 [2 n_groups, r]
+    uint8_t *mask;       // [T, n_groups]
+    float *logits;       // [T, 2 n_groups] or nullptr
+    int T, D, r, n_groups;
+    int *status;
+    int stages = 0;  // pipeline depth, set by the launcher
+};
+
 struct DecodeArgs {
     const uint16_t *x;     // bf16 [T, K]
     const uint16_t *w0;    // bf16 [N, K]  (gate, or the only weight)
@@ -69,6 +78,12 @@ cudaError_t launch_decode_mn(MNMode mode, const DecodeArgs &a, int num_sms, cuda
 // ws: fp32 partial sums, decode_k_workspace_bytes(T, K, N, G) bytes; the
 // kernel stages decode_k_smem_bytes(T, K, G) of shared memory.
 size_t decode_k_smem_bytes(int T, int K, int G);
+
+// Router (Eq. 4-5): tmX box 64 x 128 token rows of X [T, D]; tmW1 box 64 x r
+// rows of W1 [r, D].  r in {16, 32, 64}; W2 (2 n_groups x r bf16) <= 64 KB.
+bool router_supported(int r, int n_groups);
+cudaError_t launch_router(const CUtensorMap &tmX, const CUtensorMap &tmW1, const RouterArgs &a,
+                          int num_sms, cudaStream_t s);
 cudaError_t launch_decode_k(const DecodeArgs &a, float *ws, cudaStream_t s);
 size_t decode_k_workspace_bytes(int T, int K, int N, int G);
 size_t decode_mn_smem_bytes(int T, int K, int n_groups);

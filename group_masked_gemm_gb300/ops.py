@@ -60,9 +60,12 @@ def lib():
                 L.wide_gemm_k_workspace_size.restype = sz
                 L.wide_device_status.argtypes = [p]
                 L.wide_gemm_k_decode_noalloc.argtypes = [p, p, p, i, i, i, i, p, p]
+                L.wide_router_masks.argtypes = [p, p, p, i, i, i, i, p, p, p]
+                L.wide_route_and_reorder.argtypes = [p, p, p, i, i, i, i, p, p, p, p, sz, p]
                 for fn in ("wide_reorder_masks", "wide_gemm_mn_gate_up", "wide_gemm_k_down",
                            "wide_proj_mn", "wide_proj_k", "wide_device_status",
-                           "wide_gemm_k_decode_noalloc"):
+                           "wide_gemm_k_decode_noalloc", "wide_router_masks",
+                           "wide_route_and_reorder"):
                     getattr(L, fn).restype = i
                 _lib = L
     return _lib
@@ -115,6 +118,40 @@ def reorder_masks(mask, perm=None, counts=None, stream=None):
     _check("wide_reorder_masks", lib().wide_reorder_masks(
         _ptr(mask), T, ng, _ptr(perm), _ptr(counts), None, 0, _stream(stream)))
     return perm, counts
+
+
+def router_masks(X, W1, W2, mask=None, logits=False, stream=None):
+    """Eq. 4-5 router: mask [T, n_groups] (uint8) from X [T, D], W1 [r, D] and
+    W2 [2 n_groups, r] (bf16); with logits=True also the fp32 logits
+    [T, 2 n_groups] the decisions were taken on.  Returns mask or (mask, logits)."""
+    _need(X, torch.bfloat16, "X", 2)
+    _need(W1, torch.bfloat16, "W1", 2)
+    _need(W2, torch.bfloat16, "W2", 2)
+    T, D = X.shape
+    r = W1.shape[0]
+    ng = W2.shape[0] // 2
+    if mask is None:
+        mask = torch.empty((T, ng), dtype=torch.uint8, device=X.device)
+    lg = torch.empty((T, 2 * ng), dtype=torch.float32, device=X.device) if logits else None
+    _check("wide_router_masks", lib().wide_router_masks(
+        _ptr(X), _ptr(W1), _ptr(W2), T, D, r, ng, _ptr(mask), _ptr(lg), _stream(stream)))
+    return (mask, lg) if logits else mask
+
+
+def route_and_reorder(X, W1, W2, mask=None, perm=None, counts=None, stream=None):
+    """Router then mask reordering: returns (mask, perm [ng, T], counts [ng])."""
+    _need(X, torch.bfloat16, "X", 2)
+    T, D = X.shape
+    r = W1.shape[0]
+    ng = W2.shape[0] // 2
+    dev = X.device
+    mask = torch.empty((T, ng), dtype=torch.uint8, device=dev) if mask is None else mask
+    perm = torch.empty((ng, T), dtype=torch.int32, device=dev) if perm is None else perm
+    counts = torch.empty((ng,), dtype=torch.int32, device=dev) if counts is None else counts
+    _check("wide_route_and_reorder", lib().wide_route_and_reorder(
+        _ptr(X), _ptr(W1), _ptr(W2), T, D, r, ng, _ptr(mask), _ptr(perm), _ptr(counts),
+        None, 0, _stream(stream)))
+    return mask, perm, counts
 
 
 def gemm_mn_gate_up(X, W_gate, W_up, mask, perm, counts, G, out=None, stream=None):

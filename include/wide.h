@@ -81,6 +81,36 @@ wide_status_t wide_reorder_masks(const uint8_t *mask, int T, int n_groups,
 size_t wide_reorder_workspace_size(int T, int n_groups);
 
 /*
+ * Router, inference branch -- Sec. 3.1 "Routing Components", Eq. 4-5:
+ *   z[t, j]    = sum_d X[t,d] W1[j,d]              (bottleneck, j < r)
+ *   R[t, g, c] = sum_j z[t,j] W2[2g+c, j]          (X W1 W2 reshaped to [T, N_G, 2])
+ *   mask[t, g] = 1 when argmax_c R[t,g,c] = 0 (class 0 executes), i.e.
+ *                R[t,g,0] >= R[t,g,1]; a tie executes (first maximum).
+ *   X      : bf16 [T, d_model]
+ *   W1     : bf16 [r, d_model]      (the page's D x r matrix, stored [out, in])
+ *   W2     : bf16 [2 n_groups, r]   (the page's r x 2N_G matrix, stored [out, in])
+ *   mask   : uint8 [T, n_groups], written (0 or 1)
+ *   logits : float [T, 2 n_groups] (column 2g + c), written when not NULL
+ * z is accumulated in fp32 by the tensor cores and the logits are fp32 FMA
+ * sums in ascending j; the decision is taken on those fp32 logits.
+ * r in {16, 32, 64}; d_model % 64 == 0; 2 * n_groups * r * 2 <= 65536 bytes
+ * (else WIDE_ERR_UNSUPPORTED).
+ */
+wide_status_t wide_router_masks(const uint16_t *X, const uint16_t *W1, const uint16_t *W2,
+                                int T, int d_model, int r, int n_groups, uint8_t *mask,
+                                float *logits, void *stream);
+
+/*
+ * The router followed by the mask reordering of that mask (Eq. 4-5 then
+ * Eq. 7), both enqueued on `stream`: mask, perm and counts are ready for the
+ * GEMM calls.  Arguments as for wide_router_masks and wide_reorder_masks.
+ */
+wide_status_t wide_route_and_reorder(const uint16_t *X, const uint16_t *W1, const uint16_t *W2,
+                                     int T, int d_model, int r, int n_groups, uint8_t *mask,
+                                     int32_t *perm, int32_t *counts, void *ws, size_t ws_bytes,
+                                     void *stream);
+
+/*
  * FFN gate/up projection with fused activation -- Sec. 3.1 Eq. 3 (GEMM-MN,
  * App. B Algorithm 2):
  *   H[t, f] = M[t, f/G] * silu(X[t,:] . W_gate[f,:]) * (X[t,:] . W_up[f,:])
