@@ -11,6 +11,7 @@ Token-level Dynamic Width Pruning" each function restates.
 """
 from .oracle import (  # noqa: F401
     router,
+    attn_decode,
     build,
     library_path,
     reorder,

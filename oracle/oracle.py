@@ -58,6 +58,8 @@ def _load():
         lib.oracle_ffn.restype = None
         lib.oracle_router.argtypes = [p, p, p, i, i, i, i, p, p]
         lib.oracle_router.restype = None
+        lib.oracle_attn_decode.argtypes = [p, p, p, p, p, i, i, i, i, i, p]
+        lib.oracle_attn_decode.restype = None
         _lib = lib
     return _lib
 
@@ -183,3 +185,23 @@ def router(X, W1, W2):
     mask = np.empty((T, ng), np.uint8)
     _load().oracle_router(_ptr(X), _ptr(W1), _ptr(W2), T, D, r, ng, _ptr(logits), _ptr(mask))
     return logits, mask
+
+
+def attn_decode(Q, K, V, lens, mask):
+    """Routed decode attention: O [B, Hq, d] (double).
+
+    Q bf16 [B, Hq, d]; K, V bf16 [B, Hk, L_max, d]; lens int32 [B];
+    mask uint8 [B, Hk] (group g = KV head g and its Hq/Hk query heads)."""
+    Q = _c(Q, np.uint16)
+    K = _c(K, np.uint16)
+    V = _c(V, np.uint16)
+    lens = _c(lens, np.int32)
+    m = _c(mask, np.uint8)
+    B, Hq, d = Q.shape
+    _, Hk, L_max, d2 = K.shape
+    assert K.shape == V.shape and K.shape[0] == B and d2 == d and Hq % Hk == 0
+    assert lens.shape == (B,) and m.shape == (B, Hk) and (lens <= L_max).all()
+    O = np.empty((B, Hq, d), np.float64)
+    _load().oracle_attn_decode(_ptr(Q), _ptr(K), _ptr(V), _ptr(lens), _ptr(m), B, Hq, Hk, d,
+                               L_max, _ptr(O))
+    return O

@@ -17,6 +17,9 @@
  *     o_proj on in-features), G = (Hq/Hk) d.
  *   - App. B, "Implementation of GEMM-K", Eq. 21:
  *     C[m,n] = sum_g M[m,g] sum_{k in K_g} A[m,k] B[n,k].
+ *   - App. B "Implementation of Attention" (decoding paragraph) with Sec. 3.1
+ *     Eq. 2: routed decode attention, one routing group per GQA group
+ *     (G = (Hq/Hk) d), softmax(q K^T / sqrt(d)) V for active groups.
  *   - Sec. 3.1 "Routing Components", Eq. 4-5: bottleneck router
  *     R = reshape(X W1 W2) in R^{T x N_G x 2}, inference mask
  *     M = 1[argmax_c R[...,c] = 0] (class 0 executes, class 1 skips).
@@ -239,5 +242,54 @@ void oracle_router(const uint16_t *X, const uint16_t *W1, const uint16_t *W2,
             const float r1 = (float)logits[(size_t)t * nc + 2 * g + 1];
             mask[(size_t)t * n_groups + g] = (uint8_t)(r0 >= r1 ? 1 : 0);
         }
+    }
+}
+
+/*
+ * Routed decode attention (App. B "Implementation of Attention", decoding;
+ * Sec. 3.1 Eq. 2: the attention groups are GQA-aligned, G = (Hq/Hk) d, so
+ * group g is KV head g and the Hq/Hk query heads that share it).  One query
+ * token per sequence b attends to the lens[b] cached keys (the last position,
+ * so no causal cut inside the cache):
+ *   s[j]      = (q[b,h,:] . K[b,g,j,:]) / sqrt(d),   g = h / (Hq/Hk)
+ *   O[b,h,:]  = mask[b,g] * sum_j softmax(s)[j] V[b,g,j,:]
+ * An inactive group, or a sequence with no cached key, gives zeros.
+ *   Q : bf16 [B, Hq, d];  K, V : bf16 [B, Hk, L_max, d];  lens : int32 [B]
+ *   mask : uint8 [B, Hk];  O : double [B, Hq, d]
+ */
+void oracle_attn_decode(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                        const int32_t *lens, const uint8_t *mask, int B, int Hq, int Hk,
+                        int d, int L_max, double *O)
+{
+    const int qpk = Hq / Hk;
+    const double scale = 1.0 / sqrt((double)d);
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (int bh = 0; bh < B * Hq; ++bh) {
+        const int b = bh / Hq, h = bh % Hq, g = h / qpk;
+        double *o = O + (size_t)bh * d;
+        for (int e = 0; e < d; ++e) o[e] = 0.0;
+        const int L = lens[b];
+        if (mask[(size_t)b * Hk + g] == 0 || L <= 0) continue;
+        const uint16_t *q = Q + (size_t)bh * d;
+        const uint16_t *Kb = K + ((size_t)b * Hk + g) * (size_t)L_max * d;
+        const uint16_t *Vb = V + ((size_t)b * Hk + g) * (size_t)L_max * d;
+        double m = -INFINITY;
+        for (int j = 0; j < L; ++j) {
+            double sj = 0.0;
+            for (int e = 0; e < d; ++e)
+                sj += bf16_to_double(q[e]) * bf16_to_double(Kb[(size_t)j * d + e]);
+            sj *= scale;
+            if (sj > m) m = sj;
+        }
+        double l = 0.0;
+        for (int j = 0; j < L; ++j) {
+            double sj = 0.0;
+            for (int e = 0; e < d; ++e)
+                sj += bf16_to_double(q[e]) * bf16_to_double(Kb[(size_t)j * d + e]);
+            const double p = exp(sj * scale - m);
+            l += p;
+            for (int e = 0; e < d; ++e) o[e] += p * bf16_to_double(Vb[(size_t)j * d + e]);
+        }
+        for (int e = 0; e < d; ++e) o[e] /= l;
     }
 }

@@ -276,6 +276,60 @@ def test_router_tokens_are_independent():
     np.testing.assert_array_equal(mask_p, mask[order])
 
 
+def test_attn_decode_golden():
+    with open(os.path.join(GOLDEN, "attn_decode_example.json")) as f:
+        gold = json.load(f)
+    Q, K, V = (syn.bf16_bits(np.array(gold[k], np.float32)) for k in ("Q", "K", "V"))
+    O = oracle.attn_decode(Q, K, V, np.array(gold["lens"], np.int32), np.array(gold["mask"], np.uint8))
+    np.testing.assert_allclose(O, np.array(gold["O"], np.float64), rtol=1e-12, atol=1e-15)
+
+
+def _attn_inputs(seed, B=3, Hq=8, Hk=2, d=64, L_max=50):
+    rng = np.random.default_rng(seed)
+    Q = syn.bf16_bits(rng.standard_normal((B, Hq, d), dtype=np.float32))
+    K = syn.bf16_bits(rng.standard_normal((B, Hk, L_max, d), dtype=np.float32))
+    V = syn.bf16_bits(rng.standard_normal((B, Hk, L_max, d), dtype=np.float32))
+    lens = rng.integers(1, L_max + 1, size=B).astype(np.int32)
+    return Q, K, V, lens
+
+
+def test_attn_decode_key_permutation_and_tail():
+    """Softmax attention is invariant to permuting the cached (key, value)
+    pairs, and nothing past lens[b] is read."""
+    Q, K, V, lens = _attn_inputs(31)
+    mask = np.ones((Q.shape[0], K.shape[1]), np.uint8)
+    O = oracle.attn_decode(Q, K, V, lens, mask)
+    K2, V2 = K.copy(), V.copy()
+    rng = np.random.default_rng(2)
+    for b, L in enumerate(lens):
+        p = rng.permutation(L)
+        K2[b, :, :L] = K[b, :, p].transpose(1, 0, 2)
+        V2[b, :, :L] = V[b, :, p].transpose(1, 0, 2)
+        K2[b, :, L:] = 0x7F80  # +inf bit patterns past the end
+        V2[b, :, L:] = 0x7F80
+    np.testing.assert_allclose(oracle.attn_decode(Q, K2, V2, lens, mask), O, rtol=1e-12, atol=1e-13)
+
+
+def test_attn_decode_equal_keys_average_and_groups():
+    """Equal keys give uniform weights (the mean of the value rows); query
+    heads of one GQA group share its KV head; an inactive group is zero."""
+    Q, K, V, lens = _attn_inputs(32)
+    K[:] = K[:, :, :1, :]
+    mask = np.ones((Q.shape[0], K.shape[1]), np.uint8)
+    O = oracle.attn_decode(Q, K, V, lens, mask)
+    Vf = syn.bf16_to_f32(V).astype(np.float64)
+    qpk = Q.shape[1] // K.shape[1]
+    for b, L in enumerate(lens):
+        for h in range(Q.shape[1]):
+            np.testing.assert_allclose(O[b, h], Vf[b, h // qpk, :L].mean(0), rtol=1e-10, atol=1e-12)
+    Q2 = Q.copy()
+    Q2[:, 1] = Q2[:, 0]  # heads 0 and 1 share KV head 0
+    mask[1, 1] = 0
+    O2 = oracle.attn_decode(Q2, K, V, lens, mask)
+    np.testing.assert_array_equal(O2[:, 0], O2[:, 1])
+    assert (O2[1, qpk:2 * qpk] == 0).all()
+
+
 # --- invariants ---------------------------------------------------------------------
 
 def test_complement_linearity(tiny):
