@@ -269,6 +269,35 @@ wide_status_t wide_router_masks(const uint16_t *X, const uint16_t *W1, const uin
     return from_cuda(wide::launch_router(tmX, tmW1, a, ctx.num_sms, static_cast<cudaStream_t>(stream)));
 }
 
+size_t wide_attn_decode_workspace_size(int B, int Hq, int d, int L_max) {
+    if (B < 1 || Hq < 1 || d < 1 || L_max < 1) return 0;
+    return wide::attn_decode_workspace_bytes(B, Hq, d, L_max);
+}
+
+wide_status_t wide_attn_decode(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                               const int32_t *lens, const uint8_t *mask, int B, int Hq, int Hk,
+                               int d, int L_max, uint16_t *O, void *ws, size_t ws_bytes,
+                               void *stream) {
+    if (!good_ptr(Q) || !good_ptr(K) || !good_ptr(V) || !good_ptr(lens) || !good_ptr(mask) ||
+        !good_ptr(O))
+        return WIDE_ERR_INVALID_ARG;
+    if (B < 1 || B > 65535 || Hq < 1 || Hk < 1 || Hk > 65535 || L_max < 1 || Hq % Hk)
+        return WIDE_ERR_INVALID_ARG;
+    if (!wide::attn_decode_supported(Hq, Hk, d, L_max)) return WIDE_ERR_UNSUPPORTED;
+    const size_t need = wide::attn_decode_workspace_bytes(B, Hq, d, L_max);
+    if (ws == nullptr || ws_bytes < need) return WIDE_ERR_WORKSPACE;
+    if (!aligned16(ws)) return WIDE_ERR_INVALID_ARG;
+    DeviceCtx ctx;
+    wide_status_t st = device_ctx(&ctx);
+    if (st != WIDE_OK) return st;
+    float *ws_ml = static_cast<float *>(ws);
+    float *ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) +
+                                            wide::attn_decode_ml_bytes(B, Hq, L_max));
+    wide::AttnDecodeArgs a{Q,  K,  V,     lens, mask, O, ws_ml, ws_o, B, Hq, Hk, d, L_max,
+                           wide::attn_decode_chunks(L_max), ctx.status};
+    return from_cuda(wide::launch_attn_decode(a, ctx.num_sms, static_cast<cudaStream_t>(stream)));
+}
+
 wide_status_t wide_route_and_reorder(const uint16_t *X, const uint16_t *W1, const uint16_t *W2,
                                      int T, int d_model, int r, int n_groups, uint8_t *mask,
                                      int32_t *perm, int32_t *counts, void *ws, size_t ws_bytes,

@@ -42,6 +42,18 @@ struct RouterArgs {
     int stages = 0;  // pipeline depth, set by the launcher
 };
 
+struct AttnDecodeArgs {
+    const uint16_t *Q;      // bf16 [B, Hq, d]
+    const uint16_t *K, *V;  // bf16 [B, Hk, L_max, d]
+    const int32_t *lens;    // [B] cached keys per sequence
+    const uint8_t *mask;    // [B, Hk] one routing group per KV head
+    uint16_t *O;            // bf16 [B, Hq, d]
+    float *ws_ml;           // [B, Hq, n_chunks][2]: chunk max and sum
+    float *ws_o;            // [B, Hq, n_chunks][d]: chunk numerators
+    int B, Hq, Hk, d, L_max, n_chunks;
+    int *status;
+};
+
 struct DecodeArgs {
     const uint16_t *x;     // bf16 [T, K]
     const uint16_t *w0;    // bf16 [N, K]  (gate, or the only weight)
@@ -78,6 +90,14 @@ cudaError_t launch_decode_mn(MNMode mode, const DecodeArgs &a, int num_sms, cuda
 // ws: fp32 partial sums, decode_k_workspace_bytes(T, K, N, G) bytes; the
 // kernel stages decode_k_smem_bytes(T, K, G) of shared memory.
 size_t decode_k_smem_bytes(int T, int K, int G);
+
+// Routed decode attention: d in {64, 128}, Hq/Hk in {1, 2, 4, 8}, at most
+// 1022 chunks of 128 keys.
+bool attn_decode_supported(int Hq, int Hk, int d, int L_max);
+int attn_decode_chunks(int L_max);
+size_t attn_decode_ml_bytes(int B, int Hq, int L_max);
+size_t attn_decode_workspace_bytes(int B, int Hq, int d, int L_max);
+cudaError_t launch_attn_decode(const AttnDecodeArgs &a, int num_sms, cudaStream_t s);
 
 // Router (Eq. 4-5): tmX box 64 x 128 token rows of X [T, D]; tmW1 box 64 x r
 // rows of W1 [r, D].  r in {16, 32, 64}; W2 (2 n_groups x r bf16) <= 64 KB.

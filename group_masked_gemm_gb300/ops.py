@@ -62,10 +62,13 @@ def lib():
                 L.wide_gemm_k_decode_noalloc.argtypes = [p, p, p, i, i, i, i, p, p]
                 L.wide_router_masks.argtypes = [p, p, p, i, i, i, i, p, p, p]
                 L.wide_route_and_reorder.argtypes = [p, p, p, i, i, i, i, p, p, p, p, sz, p]
+                L.wide_attn_decode.argtypes = [p, p, p, p, p, i, i, i, i, i, p, p, sz, p]
+                L.wide_attn_decode_workspace_size.argtypes = [i, i, i, i]
+                L.wide_attn_decode_workspace_size.restype = sz
                 for fn in ("wide_reorder_masks", "wide_gemm_mn_gate_up", "wide_gemm_k_down",
                            "wide_proj_mn", "wide_proj_k", "wide_device_status",
                            "wide_gemm_k_decode_noalloc", "wide_router_masks",
-                           "wide_route_and_reorder"):
+                           "wide_route_and_reorder", "wide_attn_decode"):
                     getattr(L, fn).restype = i
                 _lib = L
     return _lib
@@ -152,6 +155,28 @@ def route_and_reorder(X, W1, W2, mask=None, perm=None, counts=None, stream=None)
         _ptr(X), _ptr(W1), _ptr(W2), T, D, r, ng, _ptr(mask), _ptr(perm), _ptr(counts),
         None, 0, _stream(stream)))
     return mask, perm, counts
+
+
+def attn_decode(Q, K, V, lens, mask, out=None, ws=None, stream=None):
+    """Routed decode attention: O [B, Hq, d] (bf16) from Q [B, Hq, d], K/V
+    caches [B, Hk, L_max, d] (bf16), lens [B] (int32) and mask [B, Hk] (uint8;
+    group g = KV head g with its Hq/Hk query heads)."""
+    _need(Q, torch.bfloat16, "Q", 3)
+    _need(K, torch.bfloat16, "K", 4)
+    _need(V, torch.bfloat16, "V", 4)
+    _need(lens, torch.int32, "lens", 1)
+    _need(mask, torch.uint8, "mask", 2)
+    B, Hq, d = Q.shape
+    _, Hk, L_max, _ = K.shape
+    if out is None:
+        out = torch.empty((B, Hq, d), dtype=torch.bfloat16, device=Q.device)
+    need = lib().wide_attn_decode_workspace_size(B, Hq, d, L_max)
+    if ws is None:
+        ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=Q.device)
+    _check("wide_attn_decode", lib().wide_attn_decode(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(lens), _ptr(mask), B, Hq, Hk, d, L_max, _ptr(out),
+        _ptr(ws), ws.numel(), _stream(stream)))
+    return out
 
 
 def gemm_mn_gate_up(X, W_gate, W_up, mask, perm, counts, G, out=None, stream=None):

@@ -101,6 +101,28 @@ wide_status_t wide_router_masks(const uint16_t *X, const uint16_t *W1, const uin
                                 float *logits, void *stream);
 
 /*
+ * Routed decode attention -- App. B "Implementation of Attention" (decoding:
+ * routing is checked per block, split online softmax) with the GQA-aligned
+ * groups of Sec. 3.1 Eq. 2 (G = (Hq/Hk) d, so group g is KV head g and its
+ * Hq/Hk query heads).  One query token per sequence b:
+ *   O[b,h,:] = mask[b,g] * sum_j softmax_j(Q[b,h,:] . K[b,g,j,:] / sqrt(d)) V[b,g,j,:]
+ * over the first lens[b] cached keys (g = h / (Hq/Hk)); an inactive group or
+ * lens[b] <= 0 gives zeros, and the cache of an inactive group is not read.
+ *   Q    : bf16 [B, Hq, d]           K, V : bf16 [B, Hk, L_max, d]
+ *   lens : int32 [B] (device; values are clamped to [0, L_max])
+ *   mask : uint8 [B, Hk]             O    : bf16 [B, Hq, d] (written)
+ *   ws   : wide_attn_decode_workspace_size(B, Hq, d, L_max) bytes of device
+ *          memory (fp32 per-chunk partial sums), 16-byte aligned
+ * d in {64, 128}; Hq/Hk in {1, 2, 4, 8}; L_max <= 130816 (1022 chunks of 128
+ * keys) (else WIDE_ERR_UNSUPPORTED); B, Hk <= 65535.
+ */
+wide_status_t wide_attn_decode(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                               const int32_t *lens, const uint8_t *mask, int B, int Hq, int Hk,
+                               int d, int L_max, uint16_t *O, void *ws, size_t ws_bytes,
+                               void *stream);
+size_t wide_attn_decode_workspace_size(int B, int Hq, int d, int L_max);
+
+/*
  * The router followed by the mask reordering of that mask (Eq. 4-5 then
  * Eq. 7), both enqueued on `stream`: mask, perm and counts are ready for the
  * GEMM calls.  Arguments as for wide_router_masks and wide_reorder_masks.
