@@ -293,9 +293,14 @@ wide_status_t wide_attn_decode(const uint16_t *Q, const uint16_t *K, const uint1
     float *ws_ml = static_cast<float *>(ws);
     float *ws_o = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) +
                                             wide::attn_decode_ml_bytes(B, Hq, L_max));
+    const long long rows = static_cast<long long>(B) * Hk * L_max;
+    if (rows > 0x7fffffffLL) return WIDE_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
+    CUtensorMap tmK, tmV;
+    if ((st = encode_bf16_2d(&tmK, K, rows, d, 128)) != WIDE_OK) return st;
+    if ((st = encode_bf16_2d(&tmV, V, rows, d, 128)) != WIDE_OK) return st;
     wide::AttnDecodeArgs a{Q,  K,  V,     lens, mask, O, ws_ml, ws_o, B, Hq, Hk, d, L_max,
                            wide::attn_decode_chunks(L_max), ctx.status};
-    return from_cuda(wide::launch_attn_decode(a, ctx.num_sms, static_cast<cudaStream_t>(stream)));
+    return from_cuda(wide::launch_attn_decode(tmK, tmV, a, static_cast<cudaStream_t>(stream)));
 }
 
 wide_status_t wide_route_and_reorder(const uint16_t *X, const uint16_t *W1, const uint16_t *W2,

@@ -9,13 +9,14 @@
 // KV cache, and an inactive (sequence, group) pair never reads its cache.
 //
 // Split online softmax in two kernels:
-//   attn_partial: persistent CTAs walk the (sequence, KV head, 128-key chunk)
-//     items; items of an inactive group, or past lens[b], are skipped without
-//     a read.  K and V of an item arrive by two bulk copies (TMA engine) into
-//     one of two shared-memory buffers, the next item's copies running while
-//     the current one is computed; the
-//     scores of all the group's query heads come from lane-split partial dot
-//     products over eight keys at a time and a butterfly reduce-scatter; each
+//   attn_partial: one CTA per (128-key chunk, KV head, sequence); a chunk of
+//     an inactive group, or past lens[b], returns without a read.  K and V of
+//     the chunk arrive by TMA (128-byte swizzle) into shared memory.  The two
+//     products are 16 x 128 x 128 per chunk (the group's <= 8 query heads on
+//     the M side), far below tcgen05's smallest tile, so they run on the
+//     warp-level tensor-core instruction (mma.sync m16n8k16, bf16 in, fp32
+//     accumulate) with ldmatrix reads of the swizzled tiles: S = Q K^T, the
+//     chunk softmax in fp32, then O = P V with P rounded to bf16.  Each
 //     head's chunk maximum m, sum l = sum exp(s - m) and o = sum exp(s - m) v
 //     go to the workspace.
 //   attn_combine: one CTA per (query head, sequence) merges the chunks in
@@ -37,253 +38,186 @@ __device__ __forceinline__ uint16_t f32_to_bf16(float f) {
     return *reinterpret_cast<uint16_t *>(&h);
 }
 
-// p of key j for all QPK heads, one vector load (ps is [key][QPK]).
-template <int QPK>
-__device__ __forceinline__ void load_p(const float *ps, int j, float (&p)[QPK]) {
-    if constexpr (QPK == 1) {
-        p[0] = ps[j];
-    } else if constexpr (QPK == 2) {
-        const float2 v = reinterpret_cast<const float2 *>(ps)[j];
-        p[0] = v.x; p[1] = v.y;
-    } else {
-#pragma unroll
-        for (int c = 0; c < QPK / 4; ++c) {
-            const float4 v = reinterpret_cast<const float4 *>(ps + j * QPK)[c];
-            p[4 * c] = v.x; p[4 * c + 1] = v.y; p[4 * c + 2] = v.z; p[4 * c + 3] = v.w;
-        }
-    }
+// Warp-level bf16 tensor-core product D += A B (m16n8k16, fp32 accumulate).
+__device__ __forceinline__ void mma16816(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0,
+                                         uint32_t b1) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, "
+        "{%8, %9}, {%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(0u), "r"(a2), "r"(0u), "r"(b0), "r"(b1));
+}
+__device__ __forceinline__ void ldsm_x2(uint32_t addr, uint32_t &r0, uint32_t &r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x2_trans(uint32_t addr, uint32_t &r0, uint32_t &r1) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0, %1}, [%2];"
+                 : "=r"(r0), "=r"(r1) : "r"(addr));
+}
+__device__ __forceinline__ uint32_t pack2(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t *>(&v);
 }
 
-// One work item: 128 keys of one (sequence b, KV head g).  Returns false for
-// items that read nothing (inactive group, or past the sequence's keys).
-struct Item {
-    int b, g, chunk, n_keys;
-};
-
-__device__ __forceinline__ bool item_of(const AttnDecodeArgs &a, int i, Item &it) {
-    it.chunk = i % a.n_chunks;
-    const int bg = i / a.n_chunks;
-    it.g = bg % a.Hk;
-    it.b = bg / a.Hk;
-    const int L = min(max(a.lens[it.b], 0), a.L_max);  // lengths outside [0, L_max] are clamped
-    const int j0 = it.chunk * kChunk;
-    it.n_keys = min(kChunk, L - j0);
-    return a.mask[static_cast<size_t>(it.b) * a.Hk + it.g] != 0 && j0 < L;
+// Byte offset of 16-byte chunk c (of d) of key row r in a K or V tile as the
+// TMA lays it out: 64-column halves of 128 rows x 128 B, 128-byte swizzle.
+__device__ __forceinline__ uint32_t sw_off(int r, int c) {
+    return static_cast<uint32_t>((c >> 3) * (kChunk * 128) + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
-// NB = 2: persistent CTAs, the next item's copies overlap the current item's
-// compute.  NB = 1: one item per CTA, several CTAs per SM overlap instead.
-template <int D, int QPK, int NB>
+// One CTA per (128-key chunk, KV head, sequence).  The group's QPK query heads
+// are rows 0..QPK-1 of a 16-row MMA tile (rows QPK..15 are zero).
+template <int D, int QPK>
 __global__ void __launch_bounds__(kThreads)
-    attn_partial_kernel(const AttnDecodeArgs a) {
-    extern __shared__ __align__(16) uint8_t smem[];
-    constexpr int ROW = D * 2;      // bytes of a K or V row
-    constexpr int BUF = 2 * kChunk * ROW;  // K then V of one item
-    constexpr int E = D / 32;       // elements of d per lane in the score phase
+    attn_partial_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                        const AttnDecodeArgs a) {
+    extern __shared__ __align__(1024) uint8_t smem_raw[];
+    uint8_t *smem = reinterpret_cast<uint8_t *>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    constexpr int HALVES = D / 64;
+    constexpr int TILE = HALVES * kChunk * 128;  // bytes of the K (or V) tile
     constexpr int NW = kThreads / 32;
-    float *ps = reinterpret_cast<float *>(smem + NB * BUF);                   // [kChunk][QPK]
-    float *red = ps + kChunk * QPK;                                           // [kThreads][2 QPK]
-    uint64_t *bar = reinterpret_cast<uint64_t *>(red + kThreads * 2 * QPK);  // [2]
+    uint8_t *ks = smem;
+    uint8_t *vs = smem + TILE;
+    float *ps = reinterpret_cast<float *>(smem + 2 * TILE);  // [kChunk][QPK]
+    uint64_t *bar = reinterpret_cast<uint64_t *>(ps + kChunk * QPK);
+
+    const int chunk = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
+    const int L = min(max(a.lens[b], 0), a.L_max);  // lengths outside [0, L_max] are clamped
+    const int j0 = chunk * kChunk;
+    if (a.mask[static_cast<size_t>(b) * a.Hk + g] == 0 || j0 >= L) return;
+    const int n_keys = min(kChunk, L - j0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int n_items = a.B * a.Hk * a.n_chunks;
-    const int stride = static_cast<int>(gridDim.x);
+    const int gid = lane >> 2, tig = lane & 3;  // MMA fragment coordinates
 
     if (threadIdx.x == 0) {
-        mbar_init(&bar[0], 1);
-        mbar_init(&bar[1], 1);
+        mbar_init(bar, 1);
         fence_barrier_init();
+        prefetch_tmap(&tmK);
+        prefetch_tmap(&tmV);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        // rows of the [B * Hk * L_max, d] cache view; a box may run past this
+        // head's keys (rows n_keys.. are never used, and V's are zeroed below)
+        const int row = (b * a.Hk + g) * a.L_max + j0;
+        mbar_arrive_expect_tx(bar, 2 * TILE);
+#pragma unroll
+        for (int hf = 0; hf < HALVES; ++hf) {
+            tma_load_2d(ks + hf * kChunk * 128, &tmK, bar, hf * 64, row);
+            tma_load_2d(vs + hf * kChunk * 128, &tmV, bar, hf * 64, row);
+        }
+    }
+
+    // A fragments of Q (bf16 pairs; rows gid >= QPK are zero), all k-steps over d
+    uint32_t qa[D / 16][2];
+#pragma unroll
+    for (int k = 0; k < D / 16; ++k) {
+        if (gid < QPK) {
+            const uint32_t *qrow = reinterpret_cast<const uint32_t *>(
+                a.Q + (static_cast<size_t>(b) * a.Hq + g * QPK + gid) * D + k * 16);
+            qa[k][0] = qrow[tig];
+            qa[k][1] = qrow[4 + tig];
+        } else {
+            qa[k][0] = qa[k][1] = 0u;
+        }
+    }
+    int ok = 1;
+    if (lane == 0) ok = mbar_wait(bar, 0, a.status);
+    ok = __shfl_sync(0xffffffffu, ok, 0);
+    if (!__syncthreads_and(ok)) {
+        // the status word records the timeout; give the copies one more bounded
+        // wait before the CTA's shared memory is released
+        if (threadIdx.x == 0) mbar_wait(bar, 0, nullptr);
+        return;
+    }
+    // V rows past the chunk's keys hold other data: make them exact zeros
+    if (n_keys < kChunk) {
+        const int n16 = (kChunk - n_keys) * 8 * HALVES;  // 16-byte chunks to clear
+        for (int i = threadIdx.x; i < n16; i += kThreads) {
+            const int hf = i / ((kChunk - n_keys) * 8), rem = i % ((kChunk - n_keys) * 8);
+            const int r = n_keys + rem / 8, c = rem % 8;
+            *reinterpret_cast<uint4 *>(vs + hf * kChunk * 128 + r * 128 + (c << 4)) = make_uint4(0, 0, 0, 0);
+        }
+    }
+
+    // S = Q K^T / sqrt(d): warp w takes keys [32 w, 32 w + 32) (four 8-key tiles)
+    const float scale = rsqrtf(static_cast<float>(D));
+    const uint32_t ks_u = smem_u32(ks), vs_u = smem_u32(vs);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+        const int n0 = warp * 32 + t * 8;
+        float acc[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int k = 0; k < D / 16; ++k) {
+            // lanes 0..7: rows n0.., d chunk 2k; lanes 8..15: same rows, chunk 2k + 1
+            const int r = n0 + (lane & 7), c = 2 * k + ((lane >> 3) & 1);
+            uint32_t b0, b1;
+            ldsm_x2(ks_u + sw_off(r, c), b0, b1);
+            mma16816(acc, qa[k][0], qa[k][1], b0, b1);
+        }
+        if (gid < QPK) {
+            const int j = n0 + 2 * tig;
+            if (j < n_keys) ps[j * QPK + gid] = acc[0] * scale;
+            if (j + 1 < n_keys) ps[(j + 1) * QPK + gid] = acc[1] * scale;
+        }
     }
     __syncthreads();
 
-    // every thread walks the same item sequence (the mask and lens reads hit L1)
-    auto next_item = [&](int i, Item &it) {
-        while (i < n_items && !item_of(a, i, it)) i += stride;
-        return i;
-    };
-    auto issue = [&](const Item &it, int buf) {  // thread 0: K and V of `it` into buffer buf
-        const size_t off = ((static_cast<size_t>(it.b) * a.Hk + it.g) * a.L_max + it.chunk * kChunk) * D;
-        uint8_t *dst = smem + buf * BUF;
-        const uint32_t bytes = static_cast<uint32_t>(it.n_keys * ROW);
-        mbar_arrive_expect_tx(&bar[buf], 2 * bytes);
-        bulk_load_1d(dst, a.K + off, bytes, &bar[buf]);
-        bulk_load_1d(dst + kChunk * ROW, a.V + off, bytes, &bar[buf]);
-    };
-
-    Item cur, nxt;
-    int icur = next_item(blockIdx.x, cur);
-    if (threadIdx.x == 0 && icur < n_items) issue(cur, 0);
-    int inxt = icur < n_items ? next_item(icur + stride, nxt) : n_items;
-    int buf = 0;
-    uint32_t phases = 0u;                          // bit i: parity of buffer i's next completion
-    uint32_t loaded = icur < n_items ? 1u : 0u;    // bit i: copies in flight into buffer i
-    bool abort = false;
-    const float scale = rsqrtf(static_cast<float>(D));
-
-    while (icur < n_items) {
-        // prefetch the next item into the other buffer (freed at the end of the last iteration)
-        if (NB == 2 && inxt < n_items) {
-            if (threadIdx.x == 0) issue(nxt, buf ^ 1);
-            loaded |= 1u << (buf ^ 1);
+    // per head: chunk maximum, exp(s - m) and its sum; p = 0 past n_keys
+    for (int h = warp; h < QPK; h += NW) {
+        float m = -INFINITY;
+        for (int j = lane; j < n_keys; j += 32) m = fmaxf(m, ps[j * QPK + h]);
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        float l = 0.f;
+        for (int j = lane; j < kChunk; j += 32) {
+            const float p = j < n_keys ? expf(ps[j * QPK + h] - m) : 0.f;
+            ps[j * QPK + h] = p;
+            l += p;
         }
-        const uint16_t *ks = reinterpret_cast<const uint16_t *>(smem + buf * BUF);
-        const uint16_t *vs = ks + kChunk * D;
-        const int b = cur.b, g = cur.g, n_keys = cur.n_keys;
-
-        // this lane's E elements of every query head of the group, scaled by 1/sqrt(d)
-        float q[QPK][E];
 #pragma unroll
-        for (int h = 0; h < QPK; ++h) {
-            const uint16_t *qrow = a.Q + (static_cast<size_t>(b) * a.Hq + g * QPK + h) * D + lane * E;
-#pragma unroll
-            for (int e = 0; e < E; ++e) q[h][e] = __uint_as_float(static_cast<uint32_t>(qrow[e]) << 16) * scale;
-        }
-        int ok = 1;
-        if (lane == 0) ok = mbar_wait(&bar[buf], (phases >> buf) & 1u, a.status);
-        ok = __shfl_sync(0xffffffffu, ok, 0);
-        if (!__syncthreads_and(ok)) { abort = true; break; }
-        loaded &= ~(1u << buf);
-        phases ^= 1u << buf;
-
-        // Scores, eight keys per warp step: every lane forms partial dot
-        // products over its E elements for 8 keys x QPK heads, then a butterfly
-        // reduce-scatter (xor 16, 8, 4 halve the key set, xor 2, 1 finish the
-        // sum) leaves the full score of key (lane >> 2) & 7 in each lane quad.
-        for (int jb = warp * 8; jb < n_keys; jb += NW * 8) {
-            float v[8][QPK];
-#pragma unroll
-            for (int k = 0; k < 8; ++k) {
-                float kv[E];
-                const int j = min(jb + k, n_keys - 1);  // rows past n_keys are not used
-                const uint16_t *krow = ks + j * D + lane * E;  // a warp reads one whole row
-                if constexpr (E == 4) {
-                    const uint2 w = *reinterpret_cast<const uint2 *>(krow);
-                    kv[0] = __uint_as_float(w.x << 16);
-                    kv[1] = __uint_as_float(w.x & 0xFFFF0000u);
-                    kv[2] = __uint_as_float(w.y << 16);
-                    kv[3] = __uint_as_float(w.y & 0xFFFF0000u);
-                } else {
-                    const uint32_t w = *reinterpret_cast<const uint32_t *>(krow);
-                    kv[0] = __uint_as_float(w << 16);
-                    kv[1] = __uint_as_float(w & 0xFFFF0000u);
-                }
-#pragma unroll
-                for (int h = 0; h < QPK; ++h) {
-                    float sc = 0.f;
-#pragma unroll
-                    for (int e = 0; e < E; ++e) sc = fmaf(q[h][e], kv[e], sc);
-                    v[k][h] = sc;
-                }
-            }
-#pragma unroll
-            for (int step = 0; step < 3; ++step) {
-                const int m = 16 >> step;    // 16, 8, 4
-                const int half = 4 >> step;  // keys kept after this step: 4, 2, 1
-                const bool upper = (lane & m) != 0;
-#pragma unroll
-                for (int k = 0; k < half; ++k)
-#pragma unroll
-                    for (int h = 0; h < QPK; ++h) {
-                        const float send = upper ? v[k][h] : v[k + half][h];
-                        const float keep = upper ? v[k + half][h] : v[k][h];
-                        v[k][h] = keep + __shfl_xor_sync(0xffffffffu, send, m);
-                    }
-            }
-#pragma unroll
-            for (int h = 0; h < QPK; ++h) {
-                v[0][h] += __shfl_xor_sync(0xffffffffu, v[0][h], 2);
-                v[0][h] += __shfl_xor_sync(0xffffffffu, v[0][h], 1);
-            }
-            const int j = jb + ((lane >> 2) & 7);
-            if ((lane & 3) == 0 && j < n_keys) {
-#pragma unroll
-                for (int h = 0; h < QPK; ++h) ps[j * QPK + h] = v[0][h];
-            }
-        }
-        __syncthreads();
-
-        // per head: chunk maximum, exp(s - m) and its sum (warp w handles heads w, w+NW, ...)
-        for (int h = warp; h < QPK; h += NW) {
-            float m = -INFINITY;
-            for (int j = lane; j < n_keys; j += 32) m = fmaxf(m, ps[j * QPK + h]);
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-            float l = 0.f;
-            for (int j = lane; j < n_keys; j += 32) {
-                const float p = expf(ps[j * QPK + h] - m);
-                ps[j * QPK + h] = p;
-                l += p;
-            }
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-            if (lane == 0) {
-                const size_t idx = (static_cast<size_t>(b) * a.Hq + g * QPK + h) * a.n_chunks + cur.chunk;
-                a.ws_ml[2 * idx] = m;
-                a.ws_ml[2 * idx + 1] = l;
-            }
-        }
-        __syncthreads();
-
-        // o[h][e] = sum_j p[h][j] v[j][e]: a thread owns the element pair (2c, 2c+1)
-        // and one of KS key slices; the slices are added through shared memory.
-        constexpr int PAIRS = D / 2;
-        constexpr int KS = kThreads / PAIRS;
-        const int c = threadIdx.x % PAIRS, slice = threadIdx.x / PAIRS;
-        const int per = (n_keys + KS - 1) / KS;
-        const int jlo = slice * per, jhi = min(n_keys, jlo + per);
-        float acc[QPK][2];
-#pragma unroll
-        for (int h = 0; h < QPK; ++h) acc[h][0] = acc[h][1] = 0.f;
-        for (int j = jlo; j < jhi; ++j) {
-            const uint32_t w = reinterpret_cast<const uint32_t *>(vs + j * D)[c];
-            const float v0 = __uint_as_float(w << 16), v1 = __uint_as_float(w & 0xFFFF0000u);
-            float p[QPK];
-            load_p<QPK>(ps, j, p);
-#pragma unroll
-            for (int h = 0; h < QPK; ++h) {
-                acc[h][0] = fmaf(p[h], v0, acc[h][0]);
-                acc[h][1] = fmaf(p[h], v1, acc[h][1]);
-            }
-        }
-        if (slice > 0) {
-#pragma unroll
-            for (int h = 0; h < QPK; ++h) {
-                red[threadIdx.x * 2 * QPK + 2 * h] = acc[h][0];
-                red[threadIdx.x * 2 * QPK + 2 * h + 1] = acc[h][1];
-            }
-        }
-        __syncthreads();
-        if (slice == 0) {
-            for (int sl = 1; sl < KS; ++sl) {
-                const float *r = red + (sl * PAIRS + c) * 2 * QPK;
-#pragma unroll
-                for (int h = 0; h < QPK; ++h) {  // slices added in order: deterministic
-                    acc[h][0] += r[2 * h];
-                    acc[h][1] += r[2 * h + 1];
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < QPK; ++h) {
-                const size_t idx = (static_cast<size_t>(b) * a.Hq + g * QPK + h) * a.n_chunks + cur.chunk;
-                *reinterpret_cast<float2 *>(a.ws_o + idx * D + 2 * c) = make_float2(acc[h][0], acc[h][1]);
-            }
-        }
-        __syncthreads();  // buffer `buf`, ps and red are free for the next item
-
-        cur = nxt;
-        icur = inxt;
-        inxt = icur < n_items ? next_item(icur + stride, nxt) : n_items;
-        if constexpr (NB == 2) {
-            buf ^= 1;
-        } else if (icur < n_items) {  // single buffer: load the next item only now
-            if (threadIdx.x == 0) issue(cur, 0);
-            loaded |= 1u;
+        for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+        if (lane == 0) {
+            const size_t idx = (static_cast<size_t>(b) * a.Hq + g * QPK + h) * a.n_chunks + chunk;
+            a.ws_ml[2 * idx] = m;
+            a.ws_ml[2 * idx + 1] = l;
         }
     }
-    if (abort && threadIdx.x == 0) {
-        // the status word records the timeout; give copies still in flight one
-        // more bounded wait before the CTA's shared memory is released
-        for (int i = 0; i < 2; ++i)
-            if ((loaded >> i) & 1u) mbar_wait(&bar[i], (phases >> i) & 1u, nullptr);
+    __syncthreads();
+
+    // O = P V: A = P (bf16, heads x keys), B = V via transposed ldmatrix; warp
+    // w owns d columns [w * D/4, (w+1) * D/4) (D/32 eight-column tiles)
+    constexpr int NT = D / 32;
+    float o[NT][4];
+#pragma unroll
+    for (int t = 0; t < NT; ++t) o[t][0] = o[t][1] = o[t][2] = o[t][3] = 0.f;
+#pragma unroll
+    for (int k = 0; k < kChunk / 16; ++k) {
+        uint32_t a0 = 0u, a2 = 0u;
+        if (gid < QPK) {
+            const int j = k * 16 + 2 * tig;
+            a0 = pack2(ps[j * QPK + gid], ps[(j + 1) * QPK + gid]);
+            a2 = pack2(ps[(j + 8) * QPK + gid], ps[(j + 9) * QPK + gid]);
+        }
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const int n0 = warp * (D / 4) + t * 8;
+            // lanes 0..7: key rows 16k.., lanes 8..15: rows 16k+8..; the d chunk of n0
+            const int r = k * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, c = n0 >> 3;
+            uint32_t b0, b1;
+            ldsm_x2_trans(vs_u + sw_off(r, c), b0, b1);
+            mma16816(o[t], a0, a2, b0, b1);
+        }
+    }
+    if (gid < QPK) {
+        const size_t idx = (static_cast<size_t>(b) * a.Hq + g * QPK + gid) * a.n_chunks + chunk;
+#pragma unroll
+        for (int t = 0; t < NT; ++t) {
+            const int n0 = warp * (D / 4) + t * 8;
+            *reinterpret_cast<float2 *>(a.ws_o + idx * D + n0 + 2 * tig) = make_float2(o[t][0], o[t][1]);
+        }
     }
 }
 
@@ -331,30 +265,26 @@ __global__ void __launch_bounds__(kThreads)
 }
 
 template <int D, int QPK>
-cudaError_t launch_t(const AttnDecodeArgs &a, int num_sms, cudaStream_t s) {
-    // one K+V buffer per CTA, one item per CTA (several CTAs per SM), plus the
-    // chunk's p values and the slice reduction area
-    constexpr int NB = 1;
-    (void)num_sms;
-    const size_t smem = NB * (2 * kChunk * D * 2) + kChunk * QPK * 4 + kThreads * 2 * QPK * 4 + 2 * 8;
-    auto kp = attn_partial_kernel<D, QPK, NB>;
+cudaError_t launch_t(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnDecodeArgs &a,
+                     cudaStream_t s) {
+    const size_t smem = 1024 + 2 * (D / 64) * kChunk * 128 + kChunk * QPK * 4 + 16;
+    auto kp = attn_partial_kernel<D, QPK>;
     cudaError_t e = cudaFuncSetAttribute(kp, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
     if (e != cudaSuccess) return e;
-    const long long items = static_cast<long long>(a.B) * a.Hk * a.n_chunks;
-    if (items > 0x7fffffffLL) return cudaErrorInvalidValue;
-    kp<<<static_cast<int>(items), kThreads, smem, s>>>(a);
+    kp<<<dim3(a.n_chunks, a.Hk, a.B), kThreads, smem, s>>>(tmK, tmV, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     attn_combine_kernel<D><<<dim3(a.Hq, a.B), kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 template <int D>
-cudaError_t launch_d(const AttnDecodeArgs &a, int num_sms, cudaStream_t s) {
+cudaError_t launch_d(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnDecodeArgs &a,
+                     cudaStream_t s) {
     switch (a.Hq / a.Hk) {
-        case 1: return launch_t<D, 1>(a, num_sms, s);
-        case 2: return launch_t<D, 2>(a, num_sms, s);
-        case 4: return launch_t<D, 4>(a, num_sms, s);
-        case 8: return launch_t<D, 8>(a, num_sms, s);
+        case 1: return launch_t<D, 1>(tmK, tmV, a, s);
+        case 2: return launch_t<D, 2>(tmK, tmV, a, s);
+        case 4: return launch_t<D, 4>(tmK, tmV, a, s);
+        case 8: return launch_t<D, 8>(tmK, tmV, a, s);
         default: return cudaErrorInvalidValue;
     }
 }
@@ -383,9 +313,10 @@ bool attn_decode_supported(int Hq, int Hk, int d, int L_max) {
     return attn_decode_chunks(L_max) <= 1022;  // the combine stages the chunk weights
 }
 
-cudaError_t launch_attn_decode(const AttnDecodeArgs &a, int num_sms, cudaStream_t s) {
-    if (a.d == 64) return launch_d<64>(a, num_sms, s);
-    if (a.d == 128) return launch_d<128>(a, num_sms, s);
+cudaError_t launch_attn_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnDecodeArgs &a,
+                               cudaStream_t s) {
+    if (a.d == 64) return launch_d<64>(tmK, tmV, a, s);
+    if (a.d == 128) return launch_d<128>(tmK, tmV, a, s);
     return cudaErrorInvalidValue;
 }
 

@@ -97,7 +97,9 @@ bool attn_decode_supported(int Hq, int Hk, int d, int L_max);
 int attn_decode_chunks(int L_max);
 size_t attn_decode_ml_bytes(int B, int Hq, int L_max);
 size_t attn_decode_workspace_bytes(int B, int Hq, int d, int L_max);
-cudaError_t launch_attn_decode(const AttnDecodeArgs &a, int num_sms, cudaStream_t s);
+// tmK, tmV: [B * Hk * L_max, d] views of the caches, box 64 x 128, 128-byte swizzle.
+cudaError_t launch_attn_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnDecodeArgs &a,
+                               cudaStream_t s);
 
 // Router (Eq. 4-5): tmX box 64 x 128 token rows of X [T, D]; tmW1 box 64 x r
 // rows of W1 [r, D].  r in {16, 32, 64}; W2 (2 n_groups x r bf16) <= 64 KB.
