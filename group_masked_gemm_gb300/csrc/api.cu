@@ -262,6 +262,12 @@ wide_status_t wide_router_masks(const uint16_t *X, const uint16_t *W1, const uin
     DeviceCtx ctx;
     wide_status_t st = device_ctx(&ctx);
     if (st != WIDE_OK) return st;
+    if (T <= kDecodeMaxT && d_model % 512 == 0) {
+        // decode: a cluster of CUDA-core CTAs per token, each a slice of d_model
+        // (a single 128-row tensor-core tile would walk d_model serially)
+        wide::RouterArgs a{W2, mask, logits, T, d_model, r, n_groups, ctx.status};
+        return from_cuda(wide::launch_router_decode(X, W1, a, static_cast<cudaStream_t>(stream)));
+    }
     CUtensorMap tmX, tmW1;
     if ((st = encode_bf16_2d(&tmX, X, T, d_model, 128)) != WIDE_OK) return st;
     if ((st = encode_bf16_2d(&tmW1, W1, r, d_model, r)) != WIDE_OK) return st;

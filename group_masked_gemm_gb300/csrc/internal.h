@@ -104,6 +104,10 @@ cudaError_t launch_attn_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, c
 // Router (Eq. 4-5): tmX box 64 x 128 token rows of X [T, D]; tmW1 box 64 x r
 // rows of W1 [r, D].  r in {16, 32, 64}; W2 (2 n_groups x r bf16) <= 64 KB.
 bool router_supported(int r, int n_groups);
+// Decode router (T <= 16) on CUDA cores: a cluster of 8 CTAs per token, each
+// a slice of d; needs D % 512 == 0 and r <= 64.
+cudaError_t launch_router_decode(const uint16_t *X, const uint16_t *W1, const RouterArgs &a,
+                                 cudaStream_t s);
 cudaError_t launch_router(const CUtensorMap &tmX, const CUtensorMap &tmW1, const RouterArgs &a,
                           int num_sms, cudaStream_t s);
 cudaError_t launch_decode_k(const DecodeArgs &a, float *ws, cudaStream_t s);

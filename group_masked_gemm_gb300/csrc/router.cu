@@ -265,7 +265,76 @@ cudaError_t launch_t(const CUtensorMap &tmX, const CUtensorMap &tmW1, const Rout
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Decode router (T <= 16 tokens) on CUDA cores: a cluster of kDecSplit CTAs
+// per token.  CTA k forms partial z[j] over its slice of d (warp w takes
+// j = w, w + 8, ...; lanes split the slice, 16-byte loads, fixed-order warp
+// reduction); after a cluster barrier CTA 0 adds the partials in rank order
+// through distributed shared memory and forms the logits exactly as the
+// tensor-core path's epilogue does (fp32 FMAs in ascending j, ties to class 0).
+constexpr int kDecThreads = 256;
+constexpr int kDecSplit = 8;
+
+__global__ void __cluster_dims__(kDecSplit, 1, 1) __launch_bounds__(kDecThreads)
+    router_decode_kernel(const uint16_t *__restrict__ X, const uint16_t *__restrict__ W1,
+                         const RouterArgs a) {
+    __shared__ float zs[64];  // r <= 64 partial sums of this CTA's slice
+    const int t = blockIdx.x / kDecSplit;
+    const uint32_t rank = cluster_ctarank();
+    const int D = a.D, r = a.r;
+    const int slice = D / kDecSplit;  // D % 512 == 0, so slices are whole 16-byte chunks
+    const int d0 = static_cast<int>(rank) * slice;
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint4 *xrow = reinterpret_cast<const uint4 *>(X + static_cast<size_t>(t) * D + d0);
+    for (int j = warp; j < r; j += kDecThreads / 32) {
+        const uint4 *wrow = reinterpret_cast<const uint4 *>(W1 + static_cast<size_t>(j) * D + d0);
+        float acc = 0.f;
+        for (int c = lane; c < slice / 8; c += 32) {
+            const uint4 wv = wrow[c], xv = xrow[c];
+            const uint32_t ww[4] = {wv.x, wv.y, wv.z, wv.w}, xw[4] = {xv.x, xv.y, xv.z, xv.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+                acc = fmaf(__uint_as_float(xw[e] << 16), __uint_as_float(ww[e] << 16), acc);
+                acc = fmaf(__uint_as_float(xw[e] & 0xFFFF0000u), __uint_as_float(ww[e] & 0xFFFF0000u), acc);
+            }
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) acc += __shfl_xor_sync(0xffffffffu, acc, o);
+        if (lane == 0) zs[j] = acc;
+    }
+    cluster_sync();  // every CTA's partial z is in its shared memory
+    if (rank == 0) {
+        __shared__ float z[64];
+        for (int j = threadIdx.x; j < r; j += kDecThreads) {
+            float v = 0.f;
+            for (uint32_t k = 0; k < kDecSplit; ++k) v += ld_shared_cluster_f32(&zs[j], k);
+            z[j] = v;
+        }
+        __syncthreads();
+        const int ng = a.n_groups;
+        for (int g = threadIdx.x; g < ng; g += kDecThreads) {
+            const uint16_t *w0 = a.W2 + static_cast<size_t>(2 * g) * r;
+            const uint16_t *w1 = w0 + r;
+            float r0 = 0.f, r1 = 0.f;
+            for (int j = 0; j < r; ++j) {
+                r0 = fmaf(z[j], __uint_as_float(static_cast<uint32_t>(w0[j]) << 16), r0);
+                r1 = fmaf(z[j], __uint_as_float(static_cast<uint32_t>(w1[j]) << 16), r1);
+            }
+            a.mask[static_cast<size_t>(t) * ng + g] = r0 >= r1 ? 1 : 0;  // ties go to class 0
+            if (a.logits != nullptr)
+                *reinterpret_cast<float2 *>(a.logits + static_cast<size_t>(t) * 2 * ng + 2 * g) = make_float2(r0, r1);
+        }
+    }
+    cluster_sync();  // the other CTAs' shared memory is read until here
+}
+
 }  // namespace
+
+cudaError_t launch_router_decode(const uint16_t *X, const uint16_t *W1, const RouterArgs &a,
+                                 cudaStream_t s) {
+    router_decode_kernel<<<a.T * kDecSplit, kDecThreads, 0, s>>>(X, W1, a);
+    return cudaGetLastError();
+}
 
 bool router_supported(int r, int n_groups) {
     if (r != 16 && r != 32 && r != 64) return false;

@@ -91,8 +91,10 @@ size_t wide_reorder_workspace_size(int T, int n_groups);
  *   W2     : bf16 [2 n_groups, r]   (the page's r x 2N_G matrix, stored [out, in])
  *   mask   : uint8 [T, n_groups], written (0 or 1)
  *   logits : float [T, 2 n_groups] (column 2g + c), written when not NULL
- * z is accumulated in fp32 by the tensor cores and the logits are fp32 FMA
- * sums in ascending j; the decision is taken on those fp32 logits.
+ * z is accumulated in fp32 (by the tensor cores, or for T <= 16 and
+ * d_model % 512 == 0 by a cluster of 8 CUDA-core blocks per token, one slice
+ * of d_model each) and the logits are fp32 FMA sums in ascending j; the
+ * decision is taken on those fp32 logits.
  * r in {16, 32, 64}; d_model % 64 == 0; 2 * n_groups * r * 2 <= 65536 bytes
  * (else WIDE_ERR_UNSUPPORTED).
  */

@@ -53,7 +53,10 @@ def _check_router(mask_g, logits_g, logits_ref, mask_ref):
 
 @pytest.mark.parametrize("T,D,r,ng", [(64, 256, 16, 8), (300, 512, 32, 112), (1000, 4096, 32, 112),
                                       (129, 3072, 16, 64), (17, 1024, 64, 56), (50, 256, 32, 13),
-                                      (1, 4096, 32, 112)])
+                                      (1, 4096, 32, 112),
+                                      # T <= 16: the decode path (one CUDA-core block per token)
+                                      (4, 4096, 32, 8), (16, 4096, 32, 112), (7, 256, 16, 13),
+                                      (3, 512, 64, 56)])
 def test_router_parity(T, D, r, ng):
     X, W1, W2 = _router_case(T, D, r, ng, seed=T + D + r)
     mask_g, logits_g = ops.router_masks(to_dev(X), to_dev(W1), to_dev(W2), logits=True)
@@ -77,9 +80,11 @@ def test_route_and_reorder_bit_exact():
     assert (m != mask_ref).mean() <= 1e-3
 
 
-def test_router_ties_execute():
-    """Identical class rows give exactly equal logits: every group executes."""
-    X, W1, W2 = _router_case(200, 512, 32, 24, seed=3)
+@pytest.mark.parametrize("T", [200, 5])
+def test_router_ties_execute(T):
+    """Identical class rows give exactly equal logits: every group executes
+    (tensor-core path and decode path)."""
+    X, W1, W2 = _router_case(T, 512, 32, 24, seed=3)
     W2[1::2] = W2[0::2]
     mask_g, logits_g = ops.router_masks(to_dev(X), to_dev(W1), to_dev(W2), logits=True)
     ops.device_status()
