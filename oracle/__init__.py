@@ -12,6 +12,7 @@ Token-level Dynamic Width Pruning" each function restates.
 from .oracle import (  # noqa: F401
     router,
     attn_decode,
+    attn_prefill,
     build,
     library_path,
     reorder,

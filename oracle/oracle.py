@@ -60,6 +60,8 @@ def _load():
         lib.oracle_router.restype = None
         lib.oracle_attn_decode.argtypes = [p, p, p, p, p, i, i, i, i, i, p]
         lib.oracle_attn_decode.restype = None
+        lib.oracle_attn_prefill.argtypes = [p, p, p, p, i, i, i, i, i, i, p]
+        lib.oracle_attn_prefill.restype = None
         _lib = lib
     return _lib
 
@@ -204,4 +206,21 @@ def attn_decode(Q, K, V, lens, mask):
     O = np.empty((B, Hq, d), np.float64)
     _load().oracle_attn_decode(_ptr(Q), _ptr(K), _ptr(V), _ptr(lens), _ptr(m), B, Hq, Hk, d,
                                L_max, _ptr(O))
+    return O
+
+
+def attn_prefill(Q, K, V, mask, causal=True):
+    """Routed prefill attention: O [B, T, Hq, d] (double).
+
+    Q bf16 [B, T, Hq, d]; K, V bf16 [B, Hk, T, d]; mask uint8 [B, T, Hk]."""
+    Q = _c(Q, np.uint16)
+    K = _c(K, np.uint16)
+    V = _c(V, np.uint16)
+    m = _c(mask, np.uint8)
+    B, T, Hq, d = Q.shape
+    Hk = K.shape[1]
+    assert K.shape == (B, Hk, T, d) and V.shape == K.shape and Hq % Hk == 0 and m.shape == (B, T, Hk)
+    O = np.empty((B, T, Hq, d), np.float64)
+    _load().oracle_attn_prefill(_ptr(Q), _ptr(K), _ptr(V), _ptr(m), B, T, Hq, Hk, d,
+                                1 if causal else 0, _ptr(O))
     return O

@@ -20,6 +20,9 @@
  *   - App. B "Implementation of Attention" (decoding paragraph) with Sec. 3.1
  *     Eq. 2: routed decode attention, one routing group per GQA group
  *     (G = (Hq/Hk) d), softmax(q K^T / sqrt(d)) V for active groups.
+ *   - App. B "Implementation of Attention" (prefill, Algorithm 4): routed
+ *     causal attention over the query rows of active (token, group) pairs,
+ *     dense K/V, zeros for inactive rows.
  *   - Sec. 3.1 "Routing Components", Eq. 4-5: bottleneck router
  *     R = reshape(X W1 W2) in R^{T x N_G x 2}, inference mask
  *     M = 1[argmax_c R[...,c] = 0] (class 0 executes, class 1 skips).
@@ -283,6 +286,55 @@ void oracle_attn_decode(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
         }
         double l = 0.0;
         for (int j = 0; j < L; ++j) {
+            double sj = 0.0;
+            for (int e = 0; e < d; ++e)
+                sj += bf16_to_double(q[e]) * bf16_to_double(Kb[(size_t)j * d + e]);
+            const double p = exp(sj * scale - m);
+            l += p;
+            for (int e = 0; e < d; ++e) o[e] += p * bf16_to_double(Vb[(size_t)j * d + e]);
+        }
+        for (int e = 0; e < d; ++e) o[e] /= l;
+    }
+}
+
+/*
+ * Routed prefill attention (App. B "Implementation of Attention", prefill,
+ * Algorithm 4; GQA-aligned groups of Sec. 3.1 Eq. 2: query head h reads KV
+ * head g = h / (Hq/Hk), which is also its routing group):
+ *   O[b,t,h,:] = mask[b,t,g] * sum_{j <= t (causal) or all j}
+ *                softmax_j(Q[b,t,h,:] . K[b,g,j,:] / sqrt(d)) V[b,g,j,:]
+ *   Q : bf16 [B, T, Hq, d];  K, V : bf16 [B, Hk, T, d];  mask : uint8 [B, T, Hk]
+ *   O : double [B, T, Hq, d]; inactive (token, group) rows are zero.
+ */
+void oracle_attn_prefill(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                         const uint8_t *mask, int B, int T, int Hq, int Hk, int d,
+                         int causal, double *O)
+{
+    const int qpk = Hq / Hk;
+    const double scale = 1.0 / sqrt((double)d);
+    #pragma omp parallel for schedule(dynamic, 1)
+    for (long long row = 0; row < (long long)B * T * Hq; ++row) {
+        const int h = (int)(row % Hq);
+        const int t = (int)((row / Hq) % T);
+        const int b = (int)(row / ((long long)Hq * T));
+        const int g = h / qpk;
+        double *o = O + (size_t)row * d;
+        for (int e = 0; e < d; ++e) o[e] = 0.0;
+        if (mask[((size_t)b * T + t) * Hk + g] == 0) continue;
+        const uint16_t *q = Q + (size_t)row * d;
+        const uint16_t *Kb = K + ((size_t)b * Hk + g) * (size_t)T * d;
+        const uint16_t *Vb = V + ((size_t)b * Hk + g) * (size_t)T * d;
+        const int n = causal ? t + 1 : T;
+        double m = -INFINITY;
+        for (int j = 0; j < n; ++j) {
+            double sj = 0.0;
+            for (int e = 0; e < d; ++e)
+                sj += bf16_to_double(q[e]) * bf16_to_double(Kb[(size_t)j * d + e]);
+            sj *= scale;
+            if (sj > m) m = sj;
+        }
+        double l = 0.0;
+        for (int j = 0; j < n; ++j) {
             double sj = 0.0;
             for (int e = 0; e < d; ++e)
                 sj += bf16_to_double(q[e]) * bf16_to_double(Kb[(size_t)j * d + e]);

@@ -330,6 +330,44 @@ def test_attn_decode_equal_keys_average_and_groups():
     assert (O2[1, qpk:2 * qpk] == 0).all()
 
 
+def test_attn_prefill_golden():
+    with open(os.path.join(GOLDEN, "attn_prefill_example.json")) as f:
+        gold = json.load(f)
+    Q, K, V = (syn.bf16_bits(np.array(gold[k], np.float32)) for k in ("Q", "K", "V"))
+    mask = np.array(gold["mask"], np.uint8)
+    np.testing.assert_allclose(oracle.attn_prefill(Q, K, V, mask), np.array(gold["O_causal"], np.float64),
+                               rtol=1e-12, atol=1e-15)
+    ones = np.ones_like(mask)
+    np.testing.assert_allclose(oracle.attn_prefill(Q, K, V, ones)[0, 2, 0],
+                               gold["O_all_active_causal_t2"], rtol=1e-12, atol=1e-15)
+    np.testing.assert_allclose(oracle.attn_prefill(Q, K, V, ones, causal=False)[0, 0, 0],
+                               gold["O_all_active_noncausal_t0"], rtol=1e-12, atol=1e-15)
+
+
+def test_attn_prefill_causal_is_prefix_attention():
+    """Causal output at position t equals full attention over keys 0..t, and
+    matches the decode formulation (one query over a cache of t+1 keys)."""
+    rng = np.random.default_rng(41)
+    B, T, Hq, Hk, d = 2, 20, 4, 2, 32
+    Q = syn.bf16_bits(rng.standard_normal((B, T, Hq, d), dtype=np.float32))
+    K = syn.bf16_bits(rng.standard_normal((B, Hk, T, d), dtype=np.float32))
+    V = syn.bf16_bits(rng.standard_normal((B, Hk, T, d), dtype=np.float32))
+    mask = (rng.random((B, T, Hk)) < 0.6).astype(np.uint8)
+    O = oracle.attn_prefill(Q, K, V, mask)
+    for t in (0, 7, 19):
+        Ot = oracle.attn_prefill(Q[:, :t + 1].copy(), K[:, :, :t + 1].copy(), V[:, :, :t + 1].copy(),
+                                 mask[:, :t + 1].copy(), causal=False)
+        np.testing.assert_allclose(O[:, t], Ot[:, t], rtol=1e-12, atol=1e-14)
+        Od = oracle.attn_decode(Q[:, t].copy(), K, V, np.full(B, t + 1, np.int32), mask[:, t].copy())
+        np.testing.assert_allclose(O[:, t], Od, rtol=1e-12, atol=1e-14)
+    qpk = Hq // Hk
+    for b in range(B):
+        for t in range(T):
+            for g in range(Hk):
+                if mask[b, t, g] == 0:
+                    assert (O[b, t, g * qpk:(g + 1) * qpk] == 0).all()
+
+
 # --- invariants ---------------------------------------------------------------------
 
 def test_complement_linearity(tiny):
