@@ -309,6 +309,27 @@ wide_status_t wide_attn_decode(const uint16_t *Q, const uint16_t *K, const uint1
     return from_cuda(wide::launch_attn_decode(tmK, tmV, a, static_cast<cudaStream_t>(stream)));
 }
 
+wide_status_t wide_attn_prefill(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                const int32_t *perm, const int32_t *counts, int B, int T, int Hq,
+                                int Hk, int d, int causal, uint16_t *O, void *stream) {
+    if (!good_ptr(Q) || !good_ptr(K) || !good_ptr(V) || !good_ptr(perm) || !good_ptr(counts) ||
+        !good_ptr(O))
+        return WIDE_ERR_INVALID_ARG;
+    if (B < 1 || B > 65535 || T < 1 || Hq < 1 || Hq > 65535 || Hk < 1 || Hq % Hk)
+        return WIDE_ERR_INVALID_ARG;
+    if (!wide::attn_prefill_supported(Hq, Hk, d)) return WIDE_ERR_UNSUPPORTED;
+    const long long rows = static_cast<long long>(B) * Hk * T;
+    if (rows > 0x7fffffffLL - 64) return WIDE_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
+    DeviceCtx ctx;
+    wide_status_t st = device_ctx(&ctx);
+    if (st != WIDE_OK) return st;
+    CUtensorMap tmK, tmV;
+    if ((st = encode_bf16_2d(&tmK, K, rows, d, 64)) != WIDE_OK) return st;
+    if ((st = encode_bf16_2d(&tmV, V, rows, d, 64)) != WIDE_OK) return st;
+    wide::AttnPrefillArgs a{Q, perm, counts, O, B, T, Hq, Hk, d, causal != 0, ctx.status};
+    return from_cuda(wide::launch_attn_prefill(tmK, tmV, a, static_cast<cudaStream_t>(stream)));
+}
+
 wide_status_t wide_route_and_reorder(const uint16_t *X, const uint16_t *W1, const uint16_t *W2,
                                      int T, int d_model, int r, int n_groups, uint8_t *mask,
                                      int32_t *perm, int32_t *counts, void *ws, size_t ws_bytes,

@@ -54,6 +54,15 @@ struct AttnDecodeArgs {
     int *status;
 };
 
+struct AttnPrefillArgs {
+    const uint16_t *Q;       // bf16 [B, T, Hq, d]
+    const int32_t *perm;     // [B, Hk, T]: per sequence, the stable partition of mask[b] [T, Hk]
+    const int32_t *counts;   // [B, Hk]
+    uint16_t *O;             // bf16 [B, T, Hq, d]
+    int B, T, Hq, Hk, d, causal;
+    int *status;
+};
+
 struct DecodeArgs {
     const uint16_t *x;     // bf16 [T, K]
     const uint16_t *w0;    // bf16 [N, K]  (gate, or the only weight)
@@ -100,6 +109,12 @@ size_t attn_decode_workspace_bytes(int B, int Hq, int d, int L_max);
 // tmK, tmV: [B * Hk * L_max, d] views of the caches, box 64 x 128, 128-byte swizzle.
 cudaError_t launch_attn_decode(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnDecodeArgs &a,
                                cudaStream_t s);
+
+// Routed prefill attention: tmK, tmV are [B * Hk * T, d] views of K and V,
+// box 64 x 64, 128-byte swizzle; d in {64, 128}.
+bool attn_prefill_supported(int Hq, int Hk, int d);
+cudaError_t launch_attn_prefill(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnPrefillArgs &a,
+                                cudaStream_t s);
 
 // Router (Eq. 4-5): tmX box 64 x 128 token rows of X [T, D]; tmW1 box 64 x r
 // rows of W1 [r, D].  r in {16, 32, 64}; W2 (2 n_groups x r bf16) <= 64 KB.

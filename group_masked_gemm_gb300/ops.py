@@ -65,10 +65,11 @@ def lib():
                 L.wide_attn_decode.argtypes = [p, p, p, p, p, i, i, i, i, i, p, p, sz, p]
                 L.wide_attn_decode_workspace_size.argtypes = [i, i, i, i]
                 L.wide_attn_decode_workspace_size.restype = sz
+                L.wide_attn_prefill.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, p]
                 for fn in ("wide_reorder_masks", "wide_gemm_mn_gate_up", "wide_gemm_k_down",
                            "wide_proj_mn", "wide_proj_k", "wide_device_status",
                            "wide_gemm_k_decode_noalloc", "wide_router_masks",
-                           "wide_route_and_reorder", "wide_attn_decode"):
+                           "wide_route_and_reorder", "wide_attn_decode", "wide_attn_prefill"):
                     getattr(L, fn).restype = i
                 _lib = L
     return _lib
@@ -176,6 +177,32 @@ def attn_decode(Q, K, V, lens, mask, out=None, ws=None, stream=None):
     _check("wide_attn_decode", lib().wide_attn_decode(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(lens), _ptr(mask), B, Hq, Hk, d, L_max, _ptr(out),
         _ptr(ws), ws.numel(), _stream(stream)))
+    return out
+
+
+def attn_prefill(Q, K, V, mask, causal=True, perm=None, counts=None, out=None, stream=None):
+    """Routed prefill attention: O [B, T, Hq, d] (bf16) from Q [B, T, Hq, d],
+    K/V [B, Hk, T, d] (bf16) and mask [B, T, Hk] (uint8).  perm/counts, when
+    not given, are the per-sequence reorder of mask (one call per sequence)."""
+    _need(Q, torch.bfloat16, "Q", 4)
+    _need(K, torch.bfloat16, "K", 4)
+    _need(V, torch.bfloat16, "V", 4)
+    _need(mask, torch.uint8, "mask", 3)
+    B, T, Hq, d = Q.shape
+    Hk = K.shape[1]
+    if perm is None or counts is None:
+        perm = torch.empty((B, Hk, T), dtype=torch.int32, device=Q.device)
+        counts = torch.empty((B, Hk), dtype=torch.int32, device=Q.device)
+        for b in range(B):
+            # per-sequence slices need not be 16-byte aligned: reorder into fresh buffers
+            pb, cb = reorder_masks(mask[b].clone(), stream=stream)
+            perm[b].copy_(pb)
+            counts[b].copy_(cb)
+    if out is None:
+        out = torch.empty((B, T, Hq, d), dtype=torch.bfloat16, device=Q.device)
+    _check("wide_attn_prefill", lib().wide_attn_prefill(
+        _ptr(Q), _ptr(K), _ptr(V), _ptr(perm), _ptr(counts), B, T, Hq, Hk, d, 1 if causal else 0,
+        _ptr(out), _stream(stream)))
     return out
 
 

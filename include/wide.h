@@ -125,6 +125,24 @@ wide_status_t wide_attn_decode(const uint16_t *Q, const uint16_t *K, const uint1
 size_t wide_attn_decode_workspace_size(int B, int Hq, int d, int L_max);
 
 /*
+ * Routed prefill attention -- App. B "Implementation of Attention", prefill
+ * (Algorithm 4), with the GQA-aligned groups of Sec. 3.1 Eq. 2: query head h
+ * reads KV head g = h / (Hq/Hk), which is also its routing group.
+ *   O[b,t,h,:] = mask[b,t,g] * sum_j softmax_j(Q[b,t,h,:] . K[b,g,j,:] / sqrt(d)) V[b,g,j,:]
+ * over keys j <= t (causal != 0) or all T keys; inactive rows are zero.
+ *   Q      : bf16 [B, T, Hq, d]          K, V : bf16 [B, Hk, T, d]
+ *   perm, counts : for every sequence b, wide_reorder_masks() of its mask
+ *            mask[b] ([T, Hk]): perm [B, Hk, T] int32, counts [B, Hk] int32
+ *   O      : bf16 [B, T, Hq, d] (every element written)
+ * Scores and P V run on the warp-level tensor cores (bf16 in, fp32
+ * accumulate; P rounded to bf16); the softmax is online in fp32.
+ * d in {64, 128} (else WIDE_ERR_UNSUPPORTED); B, Hq <= 65535.
+ */
+wide_status_t wide_attn_prefill(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
+                                const int32_t *perm, const int32_t *counts, int B, int T, int Hq,
+                                int Hk, int d, int causal, uint16_t *O, void *stream);
+
+/*
  * The router followed by the mask reordering of that mask (Eq. 4-5 then
  * Eq. 7), both enqueued on `stream`: mask, perm and counts are ready for the
  * GEMM calls.  Arguments as for wide_router_masks and wide_reorder_masks.

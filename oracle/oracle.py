@@ -60,7 +60,7 @@ def _load():
         lib.oracle_router.restype = None
         lib.oracle_attn_decode.argtypes = [p, p, p, p, p, i, i, i, i, i, p]
         lib.oracle_attn_decode.restype = None
-        lib.oracle_attn_prefill.argtypes = [p, p, p, p, i, i, i, i, i, i, p]
+        lib.oracle_attn_prefill.argtypes = [p, p, p, p, i, i, i, i, i, i, p, i, p]
         lib.oracle_attn_prefill.restype = None
         _lib = lib
     return _lib
@@ -209,8 +209,9 @@ def attn_decode(Q, K, V, lens, mask):
     return O
 
 
-def attn_prefill(Q, K, V, mask, causal=True):
-    """Routed prefill attention: O [B, T, Hq, d] (double).
+def attn_prefill(Q, K, V, mask, causal=True, rows=None):
+    """Routed prefill attention: O [B, T, Hq, d] (double), or [B, len(rows),
+    Hq, d] for a list of token positions `rows` (every sequence, all heads).
 
     Q bf16 [B, T, Hq, d]; K, V bf16 [B, Hk, T, d]; mask uint8 [B, T, Hk]."""
     Q = _c(Q, np.uint16)
@@ -220,7 +221,8 @@ def attn_prefill(Q, K, V, mask, causal=True):
     B, T, Hq, d = Q.shape
     Hk = K.shape[1]
     assert K.shape == (B, Hk, T, d) and V.shape == K.shape and Hq % Hk == 0 and m.shape == (B, T, Hk)
-    O = np.empty((B, T, Hq, d), np.float64)
+    r, R = _rows(rows, T)
+    O = np.empty((B, R, Hq, d), np.float64)
     _load().oracle_attn_prefill(_ptr(Q), _ptr(K), _ptr(V), _ptr(m), B, T, Hq, Hk, d,
-                                1 if causal else 0, _ptr(O))
+                                1 if causal else 0, None if r is None else _ptr(r), R, _ptr(O))
     return O

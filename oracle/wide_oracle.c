@@ -308,20 +308,25 @@ void oracle_attn_decode(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
  */
 void oracle_attn_prefill(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
                          const uint8_t *mask, int B, int T, int Hq, int Hk, int d,
-                         int causal, double *O)
+                         int causal, const int32_t *rows, int n_rows, double *O)
 {
+    /* rows: optional list of n_rows token positions t to evaluate (all heads,
+       every sequence); NULL = every position.  O is [B, R, Hq, d]. */
     const int qpk = Hq / Hk;
     const double scale = 1.0 / sqrt((double)d);
+    const int R = rows ? n_rows : T;
     #pragma omp parallel for schedule(dynamic, 1)
-    for (long long row = 0; row < (long long)B * T * Hq; ++row) {
+    for (long long row = 0; row < (long long)B * R * Hq; ++row) {
         const int h = (int)(row % Hq);
-        const int t = (int)((row / Hq) % T);
-        const int b = (int)(row / ((long long)Hq * T));
+        const int i = (int)((row / Hq) % R);
+        const int b = (int)(row / ((long long)Hq * R));
+        const int t = rows ? rows[i] : i;
         const int g = h / qpk;
+        const size_t qrow = ((size_t)b * T + t) * Hq + h;
         double *o = O + (size_t)row * d;
         for (int e = 0; e < d; ++e) o[e] = 0.0;
         if (mask[((size_t)b * T + t) * Hk + g] == 0) continue;
-        const uint16_t *q = Q + (size_t)row * d;
+        const uint16_t *q = Q + qrow * d;
         const uint16_t *Kb = K + ((size_t)b * Hk + g) * (size_t)T * d;
         const uint16_t *Vb = V + ((size_t)b * Hk + g) * (size_t)T * d;
         const int n = causal ? t + 1 : T;
