@@ -203,6 +203,14 @@ wide_status_t run_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask, i
         wide::DecodeArgs a{A, W, nullptr, mask, out, T, K, N, G};
         return from_cuda(wide::launch_decode_k(a, static_cast<float *>(ws), s));
     }
+    if (wide::gemm_k_prefill_splits(T, K, N, G, ctx.num_sms) > 1) {
+        CUtensorMap tmA, tmB;
+        if ((st = encode_bf16_2d(&tmA, A, T, K, 128)) != WIDE_OK) return st;
+        if ((st = encode_bf16_2d(&tmB, W, N, K, wide::gemm_k_split_bn(N))) != WIDE_OK) return st;
+        wide::KArgs a{mask, out, T, K, N, G, ctx.status};
+        return from_cuda(
+            wide::launch_gemm_k_split(tmA, tmB, a, static_cast<float *>(ws), ctx.num_sms, s));
+    }
     const int bn = N % 256 == 0 ? 256 : N % 128 == 0 ? 128 : 64;
     CUtensorMap tmA, tmB;
     if ((st = encode_bf16_2d(&tmA, A, T, K, 128)) != WIDE_OK) return st;
@@ -359,9 +367,13 @@ wide_status_t wide_proj_mn(const uint16_t *X, const uint16_t *W, const uint8_t *
 }
 
 size_t wide_gemm_k_workspace_size(int T, int K, int N, int G) {
-    // Prefill (T > 16) reduces in TMEM and needs none; the decode path sums
-    // fp32 partials of the split reduction dimension.
-    if (T < 1 || T > kDecodeMaxT || G <= 0 || K < G || K % G) return 0;
+    // Large prefill reduces in TMEM and needs none; decode, and prefill too
+    // small to fill the SMs, sum fp32 partials of the split reduction dimension.
+    if (T < 1 || G <= 0 || K < G || K % G) return 0;
+    if (T > kDecodeMaxT) {
+        const int sms = sizing_sms();
+        return wide::gemm_k_split_workspace_bytes(T, K, N, G, sms);
+    }
     return decode_k_on_gemm_k(N) ? wide::gemm_k_decode_workspace_bytes(T, K, N, G, sizing_sms())
                                  : wide::decode_k_workspace_bytes(T, K, N, G);
 }

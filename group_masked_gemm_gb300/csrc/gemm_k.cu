@@ -212,7 +212,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ng = args.K / args.G;
     const int m_tiles = (T + BM - 1) / BM;
     const int n_tiles = args.N / BN;
-    const int splits = AR == BM ? 1 : args.splits;
+    const int splits = args.splits;
     const int n_items = m_tiles * n_tiles * splits;
     const int kb_per_group = args.G / BK;
     const bool partial_out = args.partial != nullptr;
@@ -277,16 +277,16 @@ __global__ void __launch_bounds__(kThreads, 1)
             ok = __shfl_sync(0xffffffffu, ok, 0);
             if (!ok) { *s_abort = 1; break; }
             const MaskBuf mbuf = mask_buf<C::MASK_BUF_BYTES>(mask_area, b);
-            int n_live, first = 0;
+            int n_all;
             if constexpr (AR == BM) {
-                n_live = build_tile_masks<4>(args.mask, T, ng, m0, mbuf.lanes, mbuf.live);
+                n_all = build_tile_masks<4>(args.mask, T, ng, m0, mbuf.lanes, mbuf.live);
             } else {
-                // equal contiguous shares of the live groups, one per split
-                const int n_all = build_decode_masks(args.mask, T, ng, mbuf.lanes, mbuf.live);
-                const int per = (n_all + splits - 1) / splits;
-                first = min(n_all, sp * per);
-                n_live = min(n_all, first + per) - first;
+                n_all = build_decode_masks(args.mask, T, ng, mbuf.lanes, mbuf.live);
             }
+            // equal contiguous shares of the tile's live groups, one per split
+            const int per = (n_all + splits - 1) / splits;
+            const int first = min(n_all, sp * per);
+            const int n_live = min(n_all, first + per) - first;
             if (lane == 0) {
                 *mbuf.n_live = n_live;
                 *mbuf.first = first;
@@ -470,23 +470,25 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs
 
 int gemm_k_max_groups() { return kMaxKGroups; }
 
-// Decode split count: each 128-column output tile becomes `splits` work items,
+// Split count (decode, and prefill grids too small for the SMs): each
+// 128-column output tile becomes `splits` work items,
 // each holding an equal share of the tile's live groups.  The count minimises
 // the weight bytes of the busiest CTA (items dealt round-robin over the grid,
 // all groups taken as live) plus each SM's share of the fp32 partial traffic
 // (written here, read back by the finalize kernel); ties go to fewer splits.
-int gemm_k_decode_splits(int T, int K, int N, int G, int num_sms) {
+static int split_count(int T, int K, int N, int G, int num_sms, int bn) {
     const int ng = K / G;
-    const int n_tiles = N / 128;
+    const int n_tiles = N / bn;
+    const int m_tiles = T <= 16 ? 1 : (T + BM - 1) / BM;
     double best = 0.0;
     int best_s = 1;
     for (int s = 1; s <= ng; ++s) {
         const int g = (ng + s - 1) / s;
         if ((ng + g - 1) / g != s) continue;  // same shares as a smaller split count
-        const long long items = static_cast<long long>(n_tiles) * s;
+        const long long items = static_cast<long long>(m_tiles) * n_tiles * s;
         const long long waves = (items + num_sms - 1) / num_sms;
-        const double cta_bytes = static_cast<double>(waves) * g * G * 128 * 2;
-        const double partial = static_cast<double>(s) * T * N * 8 / num_sms;
+        const double cta_bytes = static_cast<double>(waves) * g * G * bn * 2;
+        const double partial = s > 1 ? static_cast<double>(s) * T * N * 8 / num_sms : 0.0;
         const double cost = cta_bytes + partial;
         if (s == 1 || cost < best) {
             best = cost;
@@ -494,6 +496,37 @@ int gemm_k_decode_splits(int T, int K, int N, int G, int num_sms) {
         }
     }
     return best_s;
+}
+
+int gemm_k_decode_splits(int T, int K, int N, int G, int num_sms) {
+    return split_count(T, K, N, G, num_sms, 128);
+}
+
+int gemm_k_split_bn(int N) { return N % 256 == 0 ? 256 : 128; }
+
+int gemm_k_prefill_splits(int T, int K, int N, int G, int num_sms) {
+    if (T <= 16 || N % 128 != 0) return 1;
+    // splitting only pays while the unsplit grid leaves SMs idle: past that,
+    // every split adds partial traffic and item overhead to the same MMA work
+    const long long items = static_cast<long long>((T + BM - 1) / BM) * (N / gemm_k_split_bn(N));
+    if (items >= num_sms) return 1;
+    return split_count(T, K, N, G, num_sms, gemm_k_split_bn(N));
+}
+
+size_t gemm_k_split_workspace_bytes(int T, int K, int N, int G, int num_sms) {
+    const int s = gemm_k_prefill_splits(T, K, N, G, num_sms);
+    return s > 1 ? static_cast<size_t>(s) * T * N * sizeof(float) : 0;
+}
+
+cudaError_t launch_gemm_k_split(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a0,
+                                float *ws, int num_sms, cudaStream_t s) {
+    KArgs a = a0;
+    a.splits = gemm_k_prefill_splits(a.T, a.K, a.N, a.G, num_sms);
+    a.partial = ws;
+    cudaError_t e = gemm_k_split_bn(a.N) == 256 ? launch_t<256, BM>(tmA, tmB, a, num_sms, s)
+                                                : launch_t<128, BM>(tmA, tmB, a, num_sms, s);
+    if (e != cudaSuccess) return e;
+    return launch_decode_k_finalize(ws, a.splits, a.T * a.N, a.out, s);
 }
 
 size_t gemm_k_decode_workspace_bytes(int T, int K, int N, int G, int num_sms) {

@@ -91,6 +91,15 @@ cudaError_t launch_gemm_k(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB
 // CTAs: tmA box 64 x min(T,16) (a.a_rows), tmB box 64 x 128, N % 128 == 0;
 // ws: gemm_k_decode_workspace_bytes(T, K, N, G, num_sms) of fp32 partials.
 int gemm_k_decode_splits(int T, int K, int N, int G, int num_sms);
+// Prefill (T > 16) whose output-tile grid is too small for the SMs: the
+// groups are split over CTAs (same share rule and fp32 partials as decode)
+// when gemm_k_prefill_splits() > 1; tmB box 64 x gemm_k_split_bn(N) rows;
+// ws: gemm_k_split_workspace_bytes.
+int gemm_k_split_bn(int N);
+int gemm_k_prefill_splits(int T, int K, int N, int G, int num_sms);
+size_t gemm_k_split_workspace_bytes(int T, int K, int N, int G, int num_sms);
+cudaError_t launch_gemm_k_split(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a,
+                                float *ws, int num_sms, cudaStream_t s);
 size_t gemm_k_decode_workspace_bytes(int T, int K, int N, int G, int num_sms);
 cudaError_t launch_gemm_k_decode(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a,
                                  float *ws, int num_sms, cudaStream_t s);

@@ -181,7 +181,9 @@ wide_status_t wide_gemm_mn_gate_up(const uint16_t *X, const uint16_t *W_gate,
  *   ws     : device workspace of at least
  *            wide_gemm_k_workspace_size(T, d_ffn, d_model, G) bytes
  *            (may be NULL when that size is 0)
- * fp32 accumulation in ascending group order; deterministic.
+ * fp32 accumulation in ascending group order (when the groups are split over
+ * CTAs -- decode, and batches too short to fill the GPU -- ascending within
+ * each split, then the splits in order); deterministic.
  */
 wide_status_t wide_gemm_k_down(const uint16_t *H, const uint16_t *W_down,
                                const uint8_t *mask, const int32_t *perm,
@@ -211,7 +213,9 @@ wide_status_t wide_proj_k(const uint16_t *A, const uint16_t *W,
                           const int32_t *counts, int T, int K, int N, int G,
                           uint16_t *Y, void *ws, size_t ws_bytes, void *stream);
 
-/* Workspace bytes a GEMM-K call needs for these sizes (0 = none). */
+/* Workspace bytes a GEMM-K call needs for these sizes on the current device
+ * (0 = none): fp32 partial sums when the groups are split over CTAs (T <= 16,
+ * or a batch whose output-tile grid would leave SMs idle). */
 size_t wide_gemm_k_workspace_size(int T, int K, int N, int G);
 
 /*

@@ -93,7 +93,9 @@ def test_proj_mn_parity(T, K, N, G, keep):
     (517, 2048, 384, 256, 0.4), (517, 2048, 256, 512, 0.6), (200, 1024, 512, 128, 1.0),
     (200, 1024, 512, 128, 0.0), (1000, 1536, 256, 128, 0.08),
     # G = 512 (o_proj-sized groups), ragged T, all-active and all-inactive
-    (300, 2048, 512, 512, 1.0), (300, 2048, 512, 512, 0.0), (1029, 4096, 768, 512, 0.34)])
+    (300, 2048, 512, 512, 1.0), (300, 2048, 512, 512, 0.0), (1029, 4096, 768, 512, 0.34),
+    # short batches: the groups are split over CTAs with fp32 partials
+    (33, 14336, 4096, 128, 0.5), (200, 2048, 1024, 128, 0.05)])
 def test_gemm_k_parity(T, K, N, G, keep):
     rng = np.random.default_rng(T * 3 + G)
     A = _bits_dev(rng, (T, K))
