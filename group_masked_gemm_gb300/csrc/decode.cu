@@ -71,21 +71,33 @@ __global__ void __launch_bounds__(kThreads)
     const int T = a.T, K = a.K, N = a.N, G = a.G;
     const int ng = N / G;
     uint16_t *xs = reinterpret_cast<uint16_t *>(smem);                      // [T][K]
-    uint32_t *gbits = reinterpret_cast<uint32_t *>(smem + static_cast<size_t>(TM) * K * 2);
+    uint32_t *gbits = reinterpret_cast<uint32_t *>(smem + static_cast<size_t>(TM) * K * 2);  // [ng]
+    int *glist = reinterpret_cast<int *>(gbits + ng);                                          // [ng]
+    __shared__ int s_live;
 
     for (int v = threadIdx.x; v < T * K / 8; v += kThreads)
         reinterpret_cast<uint4 *>(xs)[v] = reinterpret_cast<const uint4 *>(a.x)[v];
     build_group_bits(a.mask, T, ng, 0, ng, gbits);
     __syncthreads();
+    if (threadIdx.x == 0) {  // groups some token uses, ascending
+        int c = 0;
+        for (int g = 0; g < ng; ++g)
+            if (gbits[g] != 0u) glist[c++] = g;
+        s_live = c;
+    }
+    __syncthreads();
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_warps = gridDim.x * kWarps;
-    for (int n = blockIdx.x * kWarps + warp; n < N; n += n_warps) {
+    const int gw = blockIdx.x * kWarps + warp;
+    // rows of groups no token uses: zeros, without reading their weights
+    for (int n = gw; n < N; n += n_warps)
+        if (gbits[n / G] == 0u && lane < T) a.out[static_cast<size_t>(lane) * N + n] = 0;
+    // rows of the live groups, dealt evenly over all warps of the grid
+    const int n_active = s_live * G;
+    for (int ia = gw; ia < n_active; ia += n_warps) {
+        const int n = glist[ia / G] * G + ia % G;
         const uint32_t bits = gbits[n / G];
-        if (bits == 0) {
-            if (lane < T) a.out[static_cast<size_t>(lane) * N + n] = 0;
-            continue;
-        }
         float acc0[TM], acc1[TM];
 #pragma unroll
         for (int t = 0; t < TM; ++t) acc0[t] = acc1[t] = 0.f;
@@ -234,12 +246,12 @@ __global__ void __launch_bounds__(kThreads)
 template <MNMode MODE, int TM>
 cudaError_t launch_mn_t(const DecodeArgs &a, int num_sms, cudaStream_t s) {
     auto kern = decode_mn_kernel<MODE, TM>;
-    const size_t smem = static_cast<size_t>(TM) * a.K * 2 + static_cast<size_t>(a.N / a.G) * 4;
+    const size_t smem = decode_mn_smem_bytes(a.T, a.K, a.N / a.G);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     const int rows_blocks = (a.N + kWarps - 1) / kWarps;
-    const int per_sm = smem <= 100 * 1024 ? 2 : 1;
+    const int per_sm = smem <= 100 * 1024 ? 2 : 1;  // more CTAs per SM measured slower (prologue per CTA)
     const int grid = rows_blocks < per_sm * num_sms ? rows_blocks : per_sm * num_sms;
     kern<<<grid, kThreads, smem, s>>>(a);
     return cudaGetLastError();
@@ -250,7 +262,7 @@ int tm_of(int T) { return T <= 1 ? 1 : T <= 4 ? 4 : 16; }
 }  // namespace
 
 size_t decode_mn_smem_bytes(int T, int K, int n_groups) {
-    return static_cast<size_t>(tm_of(T)) * K * 2 + static_cast<size_t>(n_groups) * 4;
+    return static_cast<size_t>(tm_of(T)) * K * 2 + static_cast<size_t>(n_groups) * 8;  // X rows, group bits, live list
 }
 
 // Groups per split of the reduction dimension: the staged slice of TM token
