@@ -191,7 +191,7 @@ wide_status_t run_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask, i
     if (T <= kDecodeMaxT && decode_k_on_gemm_k(N)) {
         CUtensorMap tmA, tmB;
         if ((st = encode_bf16_2d(&tmA, A, T, K, T < 16 ? T : 16)) != WIDE_OK) return st;
-        if ((st = encode_bf16_2d(&tmB, W, N, K, 128)) != WIDE_OK) return st;
+        if ((st = encode_bf16_2d(&tmB, W, N, K, wide::gemm_k_decode_bn(N))) != WIDE_OK) return st;
         wide::KArgs a{mask, out, T, K, N, G, ctx.status};
         a.a_rows = T < 16 ? T : 16;
         return from_cuda(

@@ -90,6 +90,7 @@ cudaError_t launch_gemm_k(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB
 // Decode (T <= 16) GEMM-K on the GEMM-K kernel with the groups split over
 // CTAs: tmA box 64 x min(T,16) (a.a_rows), tmB box 64 x 128, N % 128 == 0;
 // ws: gemm_k_decode_workspace_bytes(T, K, N, G, num_sms) of fp32 partials.
+int gemm_k_decode_bn(int N);
 int gemm_k_decode_splits(int T, int K, int N, int G, int num_sms);
 // Prefill (T > 16) whose output-tile grid is too small for the SMs: the
 // groups are split over CTAs (same share rule and fp32 partials as decode)

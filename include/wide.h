@@ -224,13 +224,15 @@ size_t wide_gemm_k_workspace_size(int T, int K, int N, int G);
  * (a memory planner that owns every device allocation, a plugin host that
  * provides no workspace, or a path where a cudaMalloc would synchronise).
  *
- * Computes exactly what wide_gemm_k_down / wide_proj_k compute for T <= 16:
+ * Computes what wide_gemm_k_down / wide_proj_k compute for T <= 16:
  *   Y[t, n] = sum_g M[t,g] sum_{k in [gG,(g+1)G)} A[t,k] W[n,k]
  * (A: bf16 [T, K]; W: bf16 [N, K]; mask: uint8 [T, K/G]; Y: bf16 [T, N]),
- * with the same kernels and the same result, but its fp32 partial sums live
- * in a fixed array of WIDE_NOALLOC_SCRATCH_BYTES inside the library (held by
- * every GPU that loads the library until the process exits) instead of a
- * caller workspace.  Nothing is allocated or freed by this call.
+ * to the same tolerance, on the CUDA-core split-K decode kernel (its
+ * summation order, and so the last bits, can differ from the workspace
+ * entry points', which use the tensor-core kernel when N % 128 == 0).  Its
+ * fp32 partial sums live in a fixed array of WIDE_NOALLOC_SCRATCH_BYTES
+ * inside the library (held by every GPU that loads the library until the
+ * process exits) instead of a caller workspace.  Nothing is allocated or freed by this call.
  *   - Sizes whose partial sums (splits x T x N x 4 bytes; 1.3 MB for
  *     T = 16, K = 14336, N = 4096, G = 128) exceed the array return
  *     WIDE_ERR_WORKSPACE; T > 16 returns WIDE_ERR_INVALID_ARG.
