@@ -273,6 +273,18 @@ __device__ __forceinline__ float ld_shared_cluster_f32(const void *local, uint32
     return v;
 }
 
+// ------------------------------------------- programmatic dependent launch --
+// Block until the grid this one depends on (the previous kernel in the
+// stream, for a launch with programmatic stream serialization) has completed
+// and its memory is visible; returns at once after a plain launch.
+__device__ __forceinline__ void griddep_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Let the next kernel in the stream, if it was launched with programmatic
+// stream serialization, be scheduled before this grid completes (it still
+// waits for this grid's results with griddep_wait).
+__device__ __forceinline__ void griddep_launch_dependents() {
+    asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 // ------------------------------------------------------------------- misc --
 __device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
     __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);

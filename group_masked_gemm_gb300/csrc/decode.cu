@@ -157,6 +157,7 @@ constexpr int kRowsPerCta = kWarps * kRowsPerWarp;
 template <int TM>
 __global__ void __launch_bounds__(kThreads)
     decode_k_partial_kernel(const DecodeArgs a, int groups_per_split, float *ws) {
+    griddep_launch_dependents();  // see launch_decode_k_finalize
     extern __shared__ __align__(16) uint8_t smem[];
     const int T = a.T, K = a.K, N = a.N, G = a.G;
     const int ng = K / G;
@@ -236,6 +237,7 @@ __global__ void __launch_bounds__(kThreads)
 // Y[t][n] = bf16( sum over splits s = 0, 1, ... of ws[s][t][n] ).
 __global__ void __launch_bounds__(kThreads)
     decode_k_finalize_kernel(const float *ws, int splits, int TN, uint16_t *out) {
+    griddep_wait();  // the partials are the previous kernel's output
     const int i = blockIdx.x * kThreads + threadIdx.x;
     if (i >= TN) return;
     float s = 0.f;
@@ -310,10 +312,21 @@ static cudaError_t launch_k_partial(const DecodeArgs &a, int gps, int splits, fl
     return cudaGetLastError();
 }
 
+// The finalize is launched as a programmatic dependent of the partial-sum
+// kernel before it (which triggers early): its launch overlaps that kernel,
+// and griddep_wait holds it until the partials are complete and visible.
 cudaError_t launch_decode_k_finalize(const float *ws, int splits, int TN, uint16_t *out,
                                      cudaStream_t s) {
-    decode_k_finalize_kernel<<<(TN + kThreads - 1) / kThreads, kThreads, 0, s>>>(ws, splits, TN, out);
-    return cudaGetLastError();
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3((TN + kThreads - 1) / kThreads);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, decode_k_finalize_kernel, ws, splits, TN, out);
 }
 
 cudaError_t launch_decode_k(const DecodeArgs &a, float *ws, cudaStream_t s) {
@@ -325,9 +338,7 @@ cudaError_t launch_decode_k(const DecodeArgs &a, float *ws, cudaStream_t s) {
     else if (a.T <= 4) e = launch_k_partial<4>(a, gps, splits, ws, s);
     else e = launch_k_partial<16>(a, gps, splits, ws, s);
     if (e != cudaSuccess) return e;
-    const int TN = a.T * a.N;
-    decode_k_finalize_kernel<<<(TN + kThreads - 1) / kThreads, kThreads, 0, s>>>(ws, splits, TN, a.out);
-    return cudaGetLastError();
+    return launch_decode_k_finalize(ws, splits, a.T * a.N, a.out, s);
 }
 
 }  // namespace wide

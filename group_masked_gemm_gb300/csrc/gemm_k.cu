@@ -241,6 +241,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(s_tmem, C::TMEM_COLS);
         tmem_relinquish();
     }
+    // the split-partial finalize (launched as a programmatic dependent) may
+    // be scheduled now; it waits for this grid before reading the partials
+    griddep_launch_dependents();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
