@@ -16,6 +16,8 @@ namespace wide {
 
 // Status codes mirrored from include/wide.h for device code.
 constexpr int kStatusTimeout = 5;
+// WIDE_ERR_CUDA: a kernel found itself launched in a shape it cannot run.
+constexpr int kStatusLaunch = 4;
 // A pipeline wait gives up after this long (ns of %globaltimer).
 constexpr unsigned long long kWaitLimitNs = 2000ull * 1000ull * 1000ull;
 
@@ -259,6 +261,11 @@ __device__ __forceinline__ uint32_t cluster_ctarank() {
     uint32_t r;
     asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
     return r;
+}
+__device__ __forceinline__ uint32_t cluster_nctarank() {
+    uint32_t n;
+    asm volatile("mov.u32 %0, %%cluster_nctarank;" : "=r"(n));
+    return n;
 }
 __device__ __forceinline__ void cluster_sync() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::

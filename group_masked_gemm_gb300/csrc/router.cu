@@ -279,6 +279,13 @@ __global__ void __cluster_dims__(kDecSplit, 1, 1) __launch_bounds__(kDecThreads)
     router_decode_kernel(const uint16_t *__restrict__ X, const uint16_t *__restrict__ W1,
                          const RouterArgs a) {
     __shared__ float zs[64];  // r <= 64 partial sums of this CTA's slice
+    // Every CTA reads its peers' shared memory: without the cluster this
+    // kernel is compiled for (a launch that dropped the cluster shape) there
+    // are no peers, so record the error, write nothing and touch no peer.
+    if (cluster_nctarank() != kDecSplit) {
+        if (threadIdx.x == 0 && a.status != nullptr) atomicCAS(a.status, 0, kStatusLaunch);
+        return;
+    }
     const int t = blockIdx.x / kDecSplit;
     const uint32_t rank = cluster_ctarank();
     const int D = a.D, r = a.r;

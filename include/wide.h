@@ -31,7 +31,10 @@
  *     launched (WIDE_ERR_INVALID_ARG / WIDE_ERR_UNSUPPORTED).  A failed
  *     launch returns WIDE_ERR_CUDA.  Kernels never trap: a pipeline wait that
  *     exceeds its time limit records WIDE_ERR_TIMEOUT in a device status word
- *     that wide_device_status() reads back.
+ *     that wide_device_status() reads back, and a kernel that finds itself
+ *     launched without the thread-block cluster it needs (as a tool that
+ *     re-launches graph nodes one by one may do) records WIDE_ERR_CUDA there
+ *     and writes no output.
  */
 #ifndef WIDE_H
 #define WIDE_H
