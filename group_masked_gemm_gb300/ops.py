@@ -314,3 +314,59 @@ def ffn_forward_host(X_host, mask_host, W_gate, W_up, W_down, G, Y_host=None, st
         Y_host = torch.empty(Y.shape, dtype=Y.dtype, pin_memory=True)
     Y_host.copy_(Y, non_blocking=True)
     return Y_host
+
+
+class HostFfnPipeline:
+    """Masked FFN over a stream of batches held in pinned HOST memory, with the
+    copies overlapped: batch i uploads on one stream while batch i-1 computes
+    and batch i-2 downloads on two others (events order each buffer's reuse).
+
+    Every batch still pays its own host->device copy of X and the mask and its
+    own device->host copy of Y; they just run beside the kernels instead of
+    between them.  ``submit`` returns at once; ``synchronize`` waits for every
+    submitted batch.  ``depth`` device buffer sets rotate (2 is enough for a
+    copy < compute pipeline)."""
+
+    def __init__(self, W_gate, W_up, W_down, G, T, depth=2):
+        dev = W_gate.device
+        F, D = W_gate.shape
+        self.W = (W_gate, W_up, W_down)
+        self.G, self.T, self.depth, self.i = G, T, depth, 0
+        self.bufs = [{"X": torch.empty((T, D), dtype=torch.bfloat16, device=dev),
+                      "mask": torch.empty((T, F // G), dtype=torch.uint8, device=dev),
+                      "H": torch.empty((T, F), dtype=torch.bfloat16, device=dev),
+                      "Y": torch.empty((T, D), dtype=torch.bfloat16, device=dev)}
+                     for _ in range(depth)]
+        self.s_in, self.s_run, self.s_out = (torch.cuda.Stream(device=dev) for _ in range(3))
+        self.uploaded = [torch.cuda.Event() for _ in range(depth)]
+        self.computed = [torch.cuda.Event() for _ in range(depth)]
+        self.downloaded = [torch.cuda.Event() for _ in range(depth)]
+        for ev in self.computed + self.downloaded:
+            ev.record(torch.cuda.current_stream(dev))
+
+    def submit(self, X_host, mask_host, Y_host):
+        b = self.i % self.depth
+        buf = self.bufs[b]
+        self.s_in.wait_event(self.computed[b])      # the buffer's last batch has been read
+        with torch.cuda.stream(self.s_in):
+            buf["X"].copy_(X_host, non_blocking=True)
+            buf["mask"].copy_(mask_host, non_blocking=True)
+            self.uploaded[b].record(self.s_in)
+        self.s_run.wait_event(self.uploaded[b])
+        self.s_run.wait_event(self.downloaded[b])    # its last Y has left the device
+        with torch.cuda.stream(self.s_run):
+            ffn_forward(buf["X"], *self.W, buf["mask"], self.G, H=buf["H"], Y=buf["Y"],
+                        stream=self.s_run)
+            self.computed[b].record(self.s_run)
+        self.s_out.wait_event(self.computed[b])
+        with torch.cuda.stream(self.s_out):
+            Y_host.copy_(buf["Y"], non_blocking=True)
+            self.downloaded[b].record(self.s_out)
+        self.i += 1
+        return Y_host
+
+    def synchronize(self):
+        self.s_out.synchronize()
+        self.s_run.synchronize()
+        self.s_in.synchronize()
+
