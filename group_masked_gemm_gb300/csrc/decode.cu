@@ -67,6 +67,9 @@ __device__ __forceinline__ void build_group_bits(const uint8_t *mask, int T, int
 template <MNMode MODE, int TM>
 __global__ void __launch_bounds__(kThreads)
     decode_mn_kernel(const DecodeArgs a) {
+    // a kernel launched after this one as a programmatic dependent (the decode
+    // GEMM-K) may set itself up now; it waits for this grid before any input
+    griddep_launch_dependents();
     extern __shared__ __align__(16) uint8_t smem[];
     const int T = a.T, K = a.K, N = a.N, G = a.G;
     const int ng = N / G;

@@ -52,6 +52,7 @@ __global__ void __launch_bounds__(kTcThreads)
     decode_mn_tc_kernel(const __grid_constant__ CUtensorMap tmW0,
                         const __grid_constant__ CUtensorMap tmW1,
                         const __grid_constant__ CUtensorMap tmX, const DecodeArgs a, int *status) {
+    griddep_launch_dependents();  // see decode_mn_kernel
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t *smem = reinterpret_cast<uint8_t *>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));

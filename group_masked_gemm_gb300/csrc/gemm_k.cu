@@ -248,6 +248,11 @@ __global__ void __launch_bounds__(kThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem_base = *s_tmem;
+    // Everything above touches no input or output.  The decode variant is
+    // launched as a programmatic dependent of the kernel before it, so its
+    // launch and set-up overlap that kernel's tail; every read of an input
+    // and every write of an output comes after this wait.
+    griddep_wait();
     // Accumulators start at zero: every MMA accumulates (lanes it skips must
     // keep the value of the groups already added).  Only the MMA issuer waits
     // for the zeroing (named barrier 1: warps 1, 3..6); the producer and the
@@ -456,7 +461,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 template <int BN, int AR>
 cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a, int num_sms,
-                     cudaStream_t s) {
+                     cudaStream_t s, bool dependent = false) {
     using C = KCfg<BN, AR>;
     auto kern = gemm_k_kernel<BN, AR>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
@@ -464,8 +469,17 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs
     const int m_tiles = (a.T + BM - 1) / BM;
     const int items = m_tiles * (a.N / BN) * a.splits;
     const int grid = items < num_sms ? items : num_sms;
-    kern<<<grid, kThreads, C::SMEM_BYTES, s>>>(tmA, tmB, a);
-    return cudaGetLastError();
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = C::SMEM_BYTES;
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = dependent ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, a);
 }
 
 
@@ -548,8 +562,9 @@ cudaError_t launch_gemm_k_decode(const CUtensorMap &tmA, const CUtensorMap &tmB,
     KArgs a = a0;
     a.splits = gemm_k_decode_splits(a.T, a.K, a.N, a.G, num_sms);
     a.partial = ws;
-    cudaError_t e = gemm_k_decode_bn(a.N) == 256 ? launch_t<256, 16>(tmA, tmB, a, num_sms, s)
-                                                 : launch_t<128, 16>(tmA, tmB, a, num_sms, s);
+    // a programmatic dependent of the kernel before it (the decode gate/up)
+    cudaError_t e = gemm_k_decode_bn(a.N) == 256 ? launch_t<256, 16>(tmA, tmB, a, num_sms, s, true)
+                                                 : launch_t<128, 16>(tmA, tmB, a, num_sms, s, true);
     if (e != cudaSuccess) return e;
     return launch_decode_k_finalize(ws, a.splits, a.T * a.N, a.out, s);
 }
