@@ -327,15 +327,19 @@ wide_status_t wide_attn_prefill(const uint16_t *Q, const uint16_t *K, const uint
         return WIDE_ERR_INVALID_ARG;
     if (!wide::attn_prefill_supported(Hq, Hk, d)) return WIDE_ERR_UNSUPPORTED;
     const long long rows = static_cast<long long>(B) * Hk * T;
-    if (rows > 0x7fffffffLL - 64) return WIDE_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
+    if (rows > 0x7fffffffLL - 128) return WIDE_ERR_UNSUPPORTED;  // TMA row coordinates are 32-bit
     DeviceCtx ctx;
     wide_status_t st = device_ctx(&ctx);
     if (st != WIDE_OK) return st;
-    CUtensorMap tmK, tmV;
-    if ((st = encode_bf16_2d(&tmK, K, rows, d, 64)) != WIDE_OK) return st;
-    if ((st = encode_bf16_2d(&tmV, V, rows, d, 64)) != WIDE_OK) return st;
     wide::AttnPrefillArgs a{Q, perm, counts, O, B, T, Hq, Hk, d, causal != 0, ctx.status};
-    return from_cuda(wide::launch_attn_prefill(tmK, tmV, a, static_cast<cudaStream_t>(stream)));
+    cudaStream_t s = static_cast<cudaStream_t>(stream);
+    // d = 128 runs on the tensor-core (tcgen05) kernel with 128-key tiles
+    const bool tc = wide::attn_prefill_tc_supported(d);
+    CUtensorMap tmK, tmV;
+    if ((st = encode_bf16_2d(&tmK, K, rows, d, tc ? 128 : 64)) != WIDE_OK) return st;
+    if ((st = encode_bf16_2d(&tmV, V, rows, d, tc ? 128 : 64)) != WIDE_OK) return st;
+    return from_cuda(tc ? wide::launch_attn_prefill_tc(tmK, tmV, a, s)
+                        : wide::launch_attn_prefill(tmK, tmV, a, s));
 }
 
 wide_status_t wide_route_and_reorder(const uint16_t *X, const uint16_t *W1, const uint16_t *W2,

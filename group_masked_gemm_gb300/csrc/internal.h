@@ -126,6 +126,12 @@ bool attn_prefill_supported(int Hq, int Hk, int d);
 cudaError_t launch_attn_prefill(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnPrefillArgs &a,
                                 cudaStream_t s);
 
+// Routed prefill attention on tcgen05 (d = 128): tmK, tmV are [B * Hk * T, d]
+// views of K and V with box 64 x 128, 128-byte swizzle.
+bool attn_prefill_tc_supported(int d);
+cudaError_t launch_attn_prefill_tc(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnPrefillArgs &a,
+                                   cudaStream_t s);
+
 // Router (Eq. 4-5): tmX box 64 x 128 token rows of X [T, D]; tmW1 box 64 x r
 // rows of W1 [r, D].  r in {16, 32, 64}; W2 (2 n_groups x r bf16) <= 64 KB.
 bool router_supported(int r, int n_groups);

@@ -62,6 +62,8 @@ def _case(B, T, Hq, Hk, d, keep, seed):
     (1, 200, 8, 2, 128, 0.0, True),     # nothing active: every row zero
     (1, 1000, 8, 8, 128, 0.05, True),   # sparse: few admitted rows per group
     (2, 130, 16, 2, 64, 0.5, True),     # 8 query heads per KV head
+    (2, 333, 8, 2, 128, 0.7, False),    # non-causal, d = 128: a key tile past T
+    (1, 2048, 4, 1, 128, 1.0, True),    # 16 key tiles, every row active
 ])
 def test_attn_prefill_parity(B, T, Hq, Hk, d, keep, causal):
     Q, K, V, mask = _case(B, T, Hq, Hk, d, keep, seed=T + Hq)
@@ -75,6 +77,22 @@ def test_attn_prefill_parity(B, T, Hq, Hk, d, keep, causal):
     ref = oracle.attn_prefill(Q, K, V, mask, causal=causal)
     ref_abs = oracle.attn_prefill(Q, K, _abs_bits(V), mask, causal=causal)
     _assert_attn_close(Og, ref, ref_abs, "attn_prefill")
+
+
+def test_attn_prefill_large_logits():
+    """Queries scaled by 8 spread the logits over tens of log2 units, so the
+    running maximum of a row keeps growing across key tiles and the kernel's
+    rescaling of the accumulated output is exercised."""
+    B, T, Hq, Hk, d = 1, 700, 8, 2, 128
+    Q, K, V, mask = _case(B, T, Hq, Hk, d, 0.6, seed=77)
+    Q = syn.bf16_bits(syn.bf16_to_f32(Q) * np.float32(8.0))
+    O = ops.attn_prefill(_dev(Q), _dev(K), _dev(V), torch.from_numpy(mask).cuda())
+    ops.device_status()
+    Og = to_f64(O)
+    assert not np.isnan(Og).any()
+    ref = oracle.attn_prefill(Q, K, V, mask)
+    ref_abs = oracle.attn_prefill(Q, K, _abs_bits(V), mask)
+    _assert_attn_close(Og, ref, ref_abs, "attn_prefill large logits")
 
 
 def test_attn_prefill_full_size_sampled_rows():
