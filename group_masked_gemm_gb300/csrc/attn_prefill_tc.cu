@@ -249,17 +249,31 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 v[e] = x;
                 mx = fmaxf(mx, x);
             }
-            // P_{j-1} has been multiplied (the P buffer is free, O is settled)
-            if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(pvdone, (j - 1) & 1, a.status))) { ok = false; break; }
-            tc_fence_after();
+            // the running maximum; a warp rescales when any of its rows grew by
+            // more than the slack (then every lane moves to its new maximum)
             const float m_new = fmaxf(m_run, mx);
+            float alpha = 1.f;
+            bool rescale = false;
             if (j == 0) {
                 m_run = m_new;
             } else if (__any_sync(0xffffffffu, m_new > m_run + kRescaleSlack)) {
-                // the warp rescales its O rows in TMEM to the new maxima
-                const float alpha = exp2f(m_run - m_new);
-                l_run *= alpha;
+                alpha = exp2f(m_run - m_new);
                 m_run = m_new;
+                rescale = true;
+            }
+            // P = exp2(x - m_run) in registers: this overlaps the tensor cores'
+            // P_{j-1} V_{j-1}
+            float sum = 0.f;
+#pragma unroll
+            for (int e = 0; e < BKV; ++e) {
+                v[e] = exp2f(v[e] - m_run);
+                sum += v[e];
+            }
+            // P_{j-1} has been multiplied (the P buffer is free, O is settled)
+            if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(pvdone, (j - 1) & 1, a.status))) { ok = false; break; }
+            tc_fence_after();
+            if (rescale) {
+                l_run *= alpha;
                 uint32_t r[32];
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
@@ -282,21 +296,13 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     *reinterpret_cast<uint4 *>(vt + swz(rr, c)) = make_uint4(0, 0, 0, 0);
                 }
             }
-            // P = exp2(x - m_run), as bf16 into the swizzled P tile (row = this thread)
-            float sum = 0.f;
+            // P as bf16 into the swizzled P tile (row = this thread)
             uint8_t *pt = smem + kPOff;
 #pragma unroll
-            for (int c = 0; c < BKV / 8; ++c) {
-                float p[8];
-#pragma unroll
-                for (int e = 0; e < 8; ++e) {
-                    p[e] = exp2f(v[c * 8 + e] - m_run);
-                    sum += p[e];
-                }
+            for (int c = 0; c < BKV / 8; ++c)
                 *reinterpret_cast<uint4 *>(pt + swz(row, c)) =
-                    make_uint4(pack_bf16x2(p[0], p[1]), pack_bf16x2(p[2], p[3]), pack_bf16x2(p[4], p[5]),
-                               pack_bf16x2(p[6], p[7]));
-            }
+                    make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
+                               pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
             l_run += sum;
             fence_proxy_async_smem();
             tc_fence_before();
