@@ -333,11 +333,12 @@ wide_status_t wide_attn_prefill(const uint16_t *Q, const uint16_t *K, const uint
     if (st != WIDE_OK) return st;
     wide::AttnPrefillArgs a{Q, perm, counts, O, B, T, Hq, Hk, d, causal != 0, ctx.status};
     cudaStream_t s = static_cast<cudaStream_t>(stream);
-    // d = 128 runs on the tensor-core (tcgen05) kernel with 128-key tiles
+    // d = 128 runs on the tensor-core (tcgen05) kernel; both kernels take
+    // 64-key tiles
     const bool tc = wide::attn_prefill_tc_supported(d);
     CUtensorMap tmK, tmV;
-    if ((st = encode_bf16_2d(&tmK, K, rows, d, tc ? 128 : 64)) != WIDE_OK) return st;
-    if ((st = encode_bf16_2d(&tmV, V, rows, d, tc ? 128 : 64)) != WIDE_OK) return st;
+    if ((st = encode_bf16_2d(&tmK, K, rows, d, 64)) != WIDE_OK) return st;
+    if ((st = encode_bf16_2d(&tmV, V, rows, d, 64)) != WIDE_OK) return st;
     return from_cuda(tc ? wide::launch_attn_prefill_tc(tmK, tmV, a, s)
                         : wide::launch_attn_prefill(tmK, tmV, a, s));
 }

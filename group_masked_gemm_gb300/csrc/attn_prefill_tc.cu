@@ -8,11 +8,15 @@
 // a CTA owns 128 consecutive entries of that list.  The tile's largest
 // position bounds the causal key range; K and V stay dense.
 //
-// Per CTA (6 warps):
-//   warp 0      TMA producer: 128-key tiles of K and of V (128-byte swizzle),
-//               two stages, separate barriers so S can start before V lands;
+// Two CTAs share an SM (about 100 KB of shared memory and 256 TMEM columns
+// each), so one CTA's softmax runs while the other's MMAs do.  Per CTA
+// (7 warps):
+//   warp 0      TMA producer of the 64-key K tiles (128-byte swizzle), two
+//               stages, each released as soon as its S product is done;
+//   warp 6      TMA producer of the 64-key V tiles, one buffer, released by
+//               its P V product;
 //   warp 1      TMEM owner and MMA issuer (one thread):
-//                 S_j = Q K_j^T  (M = 128 queries, N = 128 keys, K = 128 dims)
+//                 S_j = Q K_j^T  (M = 128 queries, N = 64 keys, K = 128 dims)
 //                 into one of two TMEM S buffers, then
 //                 O  += P_{j-1} V_{j-1} (A = P from shared memory, B = V read
 //                 MN-major straight from its TMA tile) into the TMEM O;
@@ -36,43 +40,49 @@ namespace {
 
 constexpr int D = 128;                       // head dim
 constexpr int BQ = 128;                      // gathered query rows per CTA
-constexpr int BKV = 128;                     // keys per tile
-constexpr int kThreadsTc = 192;              // 6 warps
-constexpr int TILE = BQ * D * 2;             // 32 KB: Q, one K, one V or P tile
-constexpr int HALF = TILE / 2;               // one 64-column half (128 rows x 128 B)
+constexpr int BKV = 64;                      // keys per tile
+constexpr int kThreadsTc = 224;              // 7 warps
+constexpr int QHALF = BQ * 128;              // 64-dim half of the Q tile: 128 rows x 128 B
+constexpr int QTILE = 2 * QHALF;
+constexpr int KVHALF = BKV * 128;            // 64-dim half of a K or V tile
+constexpr int KVTILE = 2 * KVHALF;
+constexpr int PTILE = BQ * 128;              // P: 128 rows x 64 keys (one swizzled half)
 constexpr int kQOff = 0;
-constexpr int kKVOff = TILE;                 // [stage][K tile, V tile]
-constexpr int kPOff = kKVOff + 2 * 2 * TILE;
-constexpr int kTokOff = kPOff + TILE;
+constexpr int kKOff = QTILE;                 // [stage] K tiles
+constexpr int kVOff = kKOff + 2 * KVTILE;    // the V tile
+constexpr int kPOff = kVOff + KVTILE;
+constexpr int kTokOff = kPOff + PTILE;
 constexpr int kBarOff = kTokOff + BQ * 4;
 constexpr int kNumBars = 14;
 constexpr int kSmemBytes = 1024 + kBarOff + kNumBars * 8 + 16;
+constexpr int kTmemCols = 256;               // S0 [0,64), S1 [64,128), O [128,256)
+constexpr int kOCol = 2 * BKV;
 constexpr float kRescaleSlack = 8.0f;        // log2 units a stale running max may lag
 
 constexpr uint32_t kIdescS = idesc_bf16_f32(BQ, BKV);
 // O += P V: B (V, N = dims, K = keys) is MN-major -- bit 16 of the descriptor
 constexpr uint32_t kIdescPV = idesc_bf16_f32(BQ, D) | (1u << 16);
 
-// Byte offset of 16-byte chunk c (of 16) of row r in a 128-row tile stored as
-// two 64-column halves with the 128-byte swizzle (the TMA layout).
-__device__ __forceinline__ uint32_t swz(int r, int c) {
-    return static_cast<uint32_t>((c >> 3) * HALF + r * 128 + (((c & 7) ^ (r & 7)) << 4));
+// Byte offset of 16-byte chunk c (of 16) of row r in a tile of 64-column
+// halves `half` bytes apart, 128-byte swizzle (the TMA layout).
+__device__ __forceinline__ uint32_t swz(int half, int r, int c) {
+    return static_cast<uint32_t>((c >> 3) * half + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
 // Shared-memory descriptor of an MN-major operand in the 128-byte swizzle:
 // 64-element rows of the contiguous (MN) dimension, one row per K index,
-// 8-row atoms 1024 B apart along K, the two 64-element MN halves HALF apart.
-__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr) {
+// 8-row atoms 1024 B apart along K, the two 64-element MN halves `half` apart.
+__device__ __forceinline__ uint64_t sw128_mnmajor_desc(uint32_t smem_addr, uint32_t half) {
     uint64_t d = 0;
     d |= static_cast<uint64_t>((smem_addr & 0x3FFFFu) >> 4);  // start address
-    d |= static_cast<uint64_t>(HALF >> 4) << 16;               // leading offset: next MN half
+    d |= static_cast<uint64_t>(half >> 4) << 16;               // leading offset: next MN half
     d |= static_cast<uint64_t>(1024 >> 4) << 32;               // stride offset: next 8 K rows
     d |= static_cast<uint64_t>(1) << 46;                       // descriptor version
     d |= static_cast<uint64_t>(2) << 61;                       // 128-byte swizzle
     return d;
 }
 
-__global__ void __launch_bounds__(kThreadsTc, 1)
+__global__ void __launch_bounds__(kThreadsTc, 2)
     attn_prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                            const AttnPrefillArgs a) {
     extern __shared__ __align__(1024) uint8_t smem_raw[];
@@ -80,7 +90,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     int *toks = reinterpret_cast<int *>(smem + kTokOff);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + kBarOff);
-    uint64_t *kfull = bars, *vfull = bars + 2, *kvempty = bars + 4;
+    uint64_t *kfull = bars, *kempty = bars + 2, *vfull = bars + 4, *vempty = bars + 5;
     uint64_t *sfull = bars + 6, *sempty = bars + 8;
     uint64_t *pfull = bars + 10, *pvdone = bars + 11, *qready = bars + 12, *final_bar = bars + 13;
     uint32_t *s_tmem = reinterpret_cast<uint32_t *>(bars + kNumBars);
@@ -106,11 +116,12 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < 2; ++s) {
             mbar_init(&kfull[s], 1);
-            mbar_init(&vfull[s], 1);
-            mbar_init(&kvempty[s], 1);
+            mbar_init(&kempty[s], 1);
             mbar_init(&sfull[s], 1);
             mbar_init(&sempty[s], 4);
         }
+        mbar_init(vfull, 1);
+        mbar_init(vempty, 1);
         mbar_init(pfull, 4);
         mbar_init(pvdone, 1);
         mbar_init(qready, 4);
@@ -121,7 +132,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         prefetch_tmap(&tmV);
     }
     if (warp == 1) {
-        tmem_alloc(s_tmem, 512);  // S0 [0,128), S1 [128,256), O [256,384)
+        tmem_alloc(s_tmem, kTmemCols);
         tmem_relinquish();
     }
     tc_fence_before();
@@ -133,27 +144,31 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     const int kv_row0 = (b * a.Hk + g) * T;  // row of key 0 in the [B * Hk * T, d] view
     const uint32_t sbase = smem_u32(smem);
 
-    if (warp == 0) {
-        // ============================ TMA producer ============================
+    if (warp == 0 || warp == 6) {
+        // ===================== TMA producers: K (warp 0), V (warp 6) =====================
         if (lane == 0) {
+            const bool is_k = warp == 0;
+            const CUtensorMap *tm = is_k ? &tmK : &tmV;
             int issued = 0;
             for (int j = 0; j < n_kv && !*s_abort; ++j) {
-                const int s = j & 1;
-                if (j >= 2 && !mbar_wait(&kvempty[s], ((j >> 1) - 1) & 1, a.status)) { *s_abort = 1; break; }
-                uint8_t *kd = smem + kKVOff + s * 2 * TILE;
+                uint64_t *full = is_k ? &kfull[j & 1] : vfull;
+                uint8_t *dst = is_k ? smem + kKOff + (j & 1) * KVTILE : smem + kVOff;
+                bool ok = true;
+                if (is_k && j >= 2) ok = mbar_wait(&kempty[j & 1], ((j >> 1) - 1) & 1, a.status);
+                if (!is_k && j >= 1) ok = mbar_wait(vempty, (j - 1) & 1, a.status);
+                if (!ok) { *s_abort = 1; break; }
                 const int row = kv_row0 + j * BKV;
-                mbar_arrive_expect_tx(&kfull[s], TILE);
-                tma_load_2d(kd, &tmK, &kfull[s], 0, row);
-                tma_load_2d(kd + HALF, &tmK, &kfull[s], 64, row);
-                mbar_arrive_expect_tx(&vfull[s], TILE);
-                tma_load_2d(kd + TILE, &tmV, &vfull[s], 0, row);
-                tma_load_2d(kd + TILE + HALF, &tmV, &vfull[s], 64, row);
+                mbar_arrive_expect_tx(full, KVTILE);
+                tma_load_2d(dst, tm, full, 0, row);
+                tma_load_2d(dst + KVHALF, tm, full, 64, row);
                 issued = j + 1;
             }
             // copies in flight must land before the CTA exits
-            for (int j = issued - 2 > 0 ? issued - 2 : 0; j < issued; ++j) {
-                mbar_wait(&kfull[j & 1], (j >> 1) & 1, nullptr);
-                mbar_wait(&vfull[j & 1], (j >> 1) & 1, nullptr);
+            if (is_k) {
+                for (int j = issued - 2 > 0 ? issued - 2 : 0; j < issued; ++j)
+                    mbar_wait(&kfull[j & 1], (j >> 1) & 1, nullptr);
+            } else if (issued > 0) {
+                mbar_wait(vfull, (issued - 1) & 1, nullptr);
             }
         }
     } else if (warp == 1) {
@@ -166,27 +181,28 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                     if (!mbar_wait(&kfull[s], (j >> 1) & 1, a.status)) { ok = false; break; }
                     if (j >= 2 && !mbar_wait(&sempty[s], ((j >> 1) - 1) & 1, a.status)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t q0 = sbase + kQOff, k0 = sbase + kKVOff + s * 2 * TILE;
+                    const uint32_t q0 = sbase + kQOff, k0 = sbase + kKOff + s * KVTILE;
 #pragma unroll
-                    for (int kk = 0; kk < D / 16; ++kk) {
-                        const uint32_t off = (kk >> 2) * HALF + (kk & 3) * 32;
-                        mma_bf16(tmem + s * BKV, sw128_kmajor_desc(q0 + off), sw128_kmajor_desc(k0 + off),
-                                 kIdescS, kk > 0 ? 1u : 0u);
-                    }
+                    for (int kk = 0; kk < D / 16; ++kk)
+                        mma_bf16(tmem + s * BKV, sw128_kmajor_desc(q0 + (kk >> 2) * QHALF + (kk & 3) * 32),
+                                 sw128_kmajor_desc(k0 + (kk >> 2) * KVHALF + (kk & 3) * 32), kIdescS,
+                                 kk > 0 ? 1u : 0u);
                     mma_commit(&sfull[s]);
+                    mma_commit(&kempty[s]);  // the K tile is no longer needed
                 }
                 if (j >= 1) {  // O += P_{j-1} V_{j-1}
-                    const int jj = j - 1, s = jj & 1;
-                    if (!mbar_wait(&vfull[s], (jj >> 1) & 1, a.status)) { ok = false; break; }
+                    const int jj = j - 1;
+                    if (!mbar_wait(vfull, jj & 1, a.status)) { ok = false; break; }
                     if (!mbar_wait(pfull, jj & 1, a.status)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t p0 = sbase + kPOff, v0 = sbase + kKVOff + s * 2 * TILE + TILE;
+                    const uint32_t p0 = sbase + kPOff, v0 = sbase + kVOff;
 #pragma unroll
                     for (int kk = 0; kk < BKV / 16; ++kk)
-                        mma_bf16(tmem + 2 * BKV, sw128_kmajor_desc(p0 + (kk >> 2) * HALF + (kk & 3) * 32),
-                                 sw128_mnmajor_desc(v0 + kk * 2048), kIdescPV, (jj > 0 || kk > 0) ? 1u : 0u);
+                        mma_bf16(tmem + kOCol, sw128_kmajor_desc(p0 + kk * 32),
+                                 sw128_mnmajor_desc(v0 + kk * 2048, KVHALF), kIdescPV,
+                                 (jj > 0 || kk > 0) ? 1u : 0u);
                     mma_commit(pvdone);
-                    mma_commit(&kvempty[s]);
+                    mma_commit(vempty);
                 }
             }
             if (!ok) *s_abort = 1;
@@ -203,11 +219,11 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
         {
             const int tok = toks[row];
             for (int c = 0; c < D / 8; ++c) {
-                const uint32_t dst = sbase + kQOff + swz(row, c);
+                const uint32_t dst = sbase + kQOff + swz(QHALF, row, c);
                 if (tok >= 0)
                     cp_async16(dst, a.Q + ((static_cast<size_t>(b) * T + tok) * a.Hq + h) * D + 8 * c);
                 else
-                    *reinterpret_cast<uint4 *>(smem + kQOff + swz(row, c)) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(smem + kQOff + swz(QHALF, row, c)) = make_uint4(0, 0, 0, 0);
             }
             cp_async_wait_all();
             fence_proxy_async_smem();
@@ -277,30 +293,30 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
                 uint32_t r[32];
 #pragma unroll 1
                 for (int c = 0; c < D / 32; ++c) {
-                    tmem_ld32(lane_addr + 2 * BKV + c * 32, r);
+                    tmem_ld32(lane_addr + kOCol + c * 32, r);
                     tmem_ld_wait();
 #pragma unroll
                     for (int e = 0; e < 32; ++e) r[e] = __float_as_uint(__uint_as_float(r[e]) * alpha);
-                    tmem_st32(lane_addr + 2 * BKV + c * 32, r);
+                    tmem_st32(lane_addr + kOCol + c * 32, r);
                 }
                 tmem_st_wait();
             }
             if (k0 + BKV > T) {
                 // the tile runs past this head's keys: its V rows there hold other
                 // data (P is 0 for them, but 0 * NaN is not 0), so zero them
-                if (!__all_sync(0xffffffffu, mbar_wait(&vfull[s], (j >> 1) & 1, a.status))) { ok = false; break; }
-                uint8_t *vt = smem + kKVOff + s * 2 * TILE + TILE;
+                if (!__all_sync(0xffffffffu, mbar_wait(vfull, j & 1, a.status))) { ok = false; break; }
+                uint8_t *vt = smem + kVOff;
                 const int first = T - k0;
                 for (int i = row; i < (BKV - first) * 16; i += BQ) {
                     const int rr = first + i / 16, c = i % 16;
-                    *reinterpret_cast<uint4 *>(vt + swz(rr, c)) = make_uint4(0, 0, 0, 0);
+                    *reinterpret_cast<uint4 *>(vt + swz(KVHALF, rr, c)) = make_uint4(0, 0, 0, 0);
                 }
             }
             // P as bf16 into the swizzled P tile (row = this thread)
             uint8_t *pt = smem + kPOff;
 #pragma unroll
             for (int c = 0; c < BKV / 8; ++c)
-                *reinterpret_cast<uint4 *>(pt + swz(row, c)) =
+                *reinterpret_cast<uint4 *>(pt + swz(PTILE, row, c)) =
                     make_uint4(pack_bf16x2(v[8 * c], v[8 * c + 1]), pack_bf16x2(v[8 * c + 2], v[8 * c + 3]),
                                pack_bf16x2(v[8 * c + 4], v[8 * c + 5]), pack_bf16x2(v[8 * c + 6], v[8 * c + 7]));
             l_run += sum;
@@ -318,7 +334,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
             uint32_t r[32];
 #pragma unroll 1
             for (int c = 0; c < D / 32; ++c) {
-                tmem_ld32(lane_addr + 2 * BKV + c * 32, r);
+                tmem_ld32(lane_addr + kOCol + c * 32, r);
                 tmem_ld_wait();
                 if (dst != nullptr) {
 #pragma unroll
@@ -339,7 +355,7 @@ __global__ void __launch_bounds__(kThreadsTc, 1)
     __syncthreads();
     if (warp == 1) {
         tc_fence_after();
-        tmem_dealloc(tmem, 512);
+        tmem_dealloc(tmem, kTmemCols);
     }
 }
 
@@ -351,6 +367,9 @@ cudaError_t launch_attn_prefill_tc(const CUtensorMap &tmK, const CUtensorMap &tm
                                    cudaStream_t s) {
     cudaError_t e = cudaFuncSetAttribute(attn_prefill_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          kSmemBytes);
+    if (e != cudaSuccess) return e;
+    // two CTAs per SM: prefer the largest shared-memory carve-out
+    e = cudaFuncSetAttribute(attn_prefill_tc_kernel, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
     if (e != cudaSuccess) return e;
     attn_prefill_tc_kernel<<<dim3((a.T + BQ - 1) / BQ, a.Hq, a.B), kThreadsTc, kSmemBytes, s>>>(tmK, tmV, a);
     return cudaGetLastError();

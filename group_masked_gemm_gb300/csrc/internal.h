@@ -127,7 +127,7 @@ cudaError_t launch_attn_prefill(const CUtensorMap &tmK, const CUtensorMap &tmV, 
                                 cudaStream_t s);
 
 // Routed prefill attention on tcgen05 (d = 128): tmK, tmV are [B * Hk * T, d]
-// views of K and V with box 64 x 128, 128-byte swizzle.
+// views of K and V with box 64 x 64, 128-byte swizzle.
 bool attn_prefill_tc_supported(int d);
 cudaError_t launch_attn_prefill_tc(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnPrefillArgs &a,
                                    cudaStream_t s);
