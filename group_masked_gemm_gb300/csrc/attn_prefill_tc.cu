@@ -254,17 +254,18 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
             if (lane == 0) mbar_arrive(&sempty[s]);  // S_j is in registers
             const int k0 = j * BKV;
             const bool cut = (a.causal && k0 + BKV - 1 > min_pos) || k0 + BKV > T;
-            float mx = -INFINITY;
+            // raw scores; the cut ones become -inf, and the row maximum (the
+            // scale is positive) runs in 4 independent chains
+            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
             for (int e = 0; e < BKV; ++e) {
-                float x = v[e] * sl2;
                 if (cut) {
                     const int kpos = k0 + e;
-                    if (kpos >= T || (a.causal && kpos > qpos)) x = -INFINITY;
+                    if (kpos >= T || (a.causal && kpos > qpos)) v[e] = -INFINITY;
                 }
-                v[e] = x;
-                mx = fmaxf(mx, x);
+                mx4[e & 3] = fmaxf(mx4[e & 3], v[e]);
             }
+            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
             // the running maximum; a warp rescales when any of its rows grew by
             // more than the slack (then every lane moves to its new maximum)
             const float m_new = fmaxf(m_run, mx);
@@ -277,14 +278,15 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
                 m_run = m_new;
                 rescale = true;
             }
-            // P = exp2(x - m_run) in registers: this overlaps the tensor cores'
-            // P_{j-1} V_{j-1}
-            float sum = 0.f;
+            // P = exp2(x - m_run) in registers, x the scaled score: this overlaps
+            // the tensor cores' P_{j-1} V_{j-1}
+            float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int e = 0; e < BKV; ++e) {
-                v[e] = exp2f(v[e] - m_run);
-                sum += v[e];
+                v[e] = exp2f(fmaf(v[e], sl2, -m_run));  // exp2(score * log2(e) / sqrt(d) - max)
+                sum4[e & 3] += v[e];
             }
+            const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
             // P_{j-1} has been multiplied (the P buffer is free, O is settled)
             if (j > 0 && !__all_sync(0xffffffffu, mbar_wait(pvdone, (j - 1) & 1, a.status))) { ok = false; break; }
             tc_fence_after();
