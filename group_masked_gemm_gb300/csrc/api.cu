@@ -343,11 +343,37 @@ wide_status_t wide_attn_prefill(const uint16_t *Q, const uint16_t *K, const uint
                         : wide::launch_attn_prefill(tmK, tmV, a, s));
 }
 
+size_t wide_route_and_reorder_workspace_size(int T, int n_groups) {
+    if (T <= kDecodeMaxT || n_groups < 1) return 0;
+    return wide::route_reorder_workspace_bytes(T, n_groups);
+}
+
 wide_status_t wide_route_and_reorder(const uint16_t *X, const uint16_t *W1, const uint16_t *W2,
                                      int T, int d_model, int r, int n_groups, uint8_t *mask,
                                      int32_t *perm, int32_t *counts, void *ws, size_t ws_bytes,
                                      void *stream) {
     if (!good_ptr(perm) || !good_ptr(counts) || n_groups > 65535) return WIDE_ERR_INVALID_ARG;
+    const size_t fused_ws = wide_route_and_reorder_workspace_size(T, n_groups);
+    if (fused_ws > 0 && ws != nullptr && ws_bytes >= fused_ws) {
+        // one cooperative launch: router, then the reorder of its mask
+        if (!good_ptr(X) || !good_ptr(W1) || !good_ptr(W2) || !good_ptr(mask) || !aligned16(ws))
+            return WIDE_ERR_INVALID_ARG;
+        if (d_model < 64 || d_model % 64 || r < 16 || r % 16) return WIDE_ERR_INVALID_ARG;
+        if (!wide::router_supported(r, n_groups)) return WIDE_ERR_UNSUPPORTED;
+        DeviceCtx ctx;
+        wide_status_t st = device_ctx(&ctx);
+        if (st != WIDE_OK) return st;
+        CUtensorMap tmX, tmW1;
+        if ((st = encode_bf16_2d(&tmX, X, T, d_model, 128)) != WIDE_OK) return st;
+        if ((st = encode_bf16_2d(&tmW1, W1, r, d_model, r)) != WIDE_OK) return st;
+        cudaStream_t s = static_cast<cudaStream_t>(stream);
+        if (cudaMemsetAsync(ws, 0, 16, s) != cudaSuccess) return WIDE_ERR_CUDA;  // grid barrier counter
+        wide::RouterArgs a{W2, mask, nullptr, T, d_model, r, n_groups, ctx.status};
+        a.perm = perm;
+        a.counts = counts;
+        a.ws = static_cast<uint32_t *>(ws);
+        return from_cuda(wide::launch_route_reorder(tmX, tmW1, a, ctx.num_sms, s));
+    }
     wide_status_t st = wide_router_masks(X, W1, W2, T, d_model, r, n_groups, mask, nullptr, stream);
     if (st != WIDE_OK) return st;
     return wide_reorder_masks(mask, T, n_groups, perm, counts, ws, ws_bytes, stream);

@@ -40,6 +40,10 @@ struct RouterArgs {
     int T, D, r, n_groups;
     int *status;
     int stages = 0;  // pipeline depth, set by the launcher
+    // fused reorder (route_and_reorder in one launch); null for the router alone
+    int32_t *perm = nullptr;     // [n_groups, T]
+    int32_t *counts = nullptr;   // [n_groups]
+    uint32_t *ws = nullptr;      // route_reorder_workspace_bytes(T, n_groups), barrier word zeroed
 };
 
 struct AttnDecodeArgs {
@@ -139,6 +143,12 @@ bool router_supported(int r, int n_groups);
 // a slice of d; needs D % 512 == 0 and r <= 64.
 cudaError_t launch_router_decode(const uint16_t *X, const uint16_t *W1, const RouterArgs &a,
                                  cudaStream_t s);
+// Router and mask reordering in one cooperative launch (T > 16): a.perm,
+// a.counts and a.ws set; the first 16 bytes of a.ws must be zero (a grid
+// barrier counter).
+size_t route_reorder_workspace_bytes(int T, int n_groups);
+cudaError_t launch_route_reorder(const CUtensorMap &tmX, const CUtensorMap &tmW1, const RouterArgs &a,
+                                 int num_sms, cudaStream_t s);
 cudaError_t launch_router(const CUtensorMap &tmX, const CUtensorMap &tmW1, const RouterArgs &a,
                           int num_sms, cudaStream_t s);
 cudaError_t launch_decode_k(const DecodeArgs &a, float *ws, cudaStream_t s);

@@ -15,6 +15,16 @@
 // fp32 FMAs in ascending j against W2 held in shared memory (four groups at
 // a time, eight independent chains), and write the mask row (and optionally
 // the logits).
+//
+// route_reorder (REORDER = true) adds the mask reordering (Eq. 7) to the same
+// launch.  The epilogue warps also ballot every group's decisions over their
+// 32 token rows and store the four ballots of each (tile, group) in the
+// workspace; after a grid barrier each CTA scans one group's per-tile active
+// counts into tile offsets and counts[g]; after a second barrier each CTA
+// places the tokens of its own tiles: active token at offset + rank among the
+// tile's active tokens, inactive token after counts[g] likewise -- the stable
+// partition, bit for bit.  The launch is cooperative (every CTA resident), and
+// the barriers are bounded waits on a counter in the workspace.
 #include "common.cuh"
 #include "internal.h"
 
@@ -51,7 +61,61 @@ struct RouterCfg {
     }
 };
 
-template <int R>
+// Exclusive scan of v over the block; *total receives the block sum.
+__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    int inc = v;
+#pragma unroll
+    for (int d = 1; d < 32; d <<= 1) {
+        const int y = __shfl_up_sync(0xffffffffu, inc, d);
+        if (lane >= d) inc += y;
+    }
+    if (lane == 31) warp_sums[warp] = inc;
+    __syncthreads();
+    if (warp == 0) {
+        const int nw = blockDim.x >> 5;
+        const int w = lane < nw ? warp_sums[lane] : 0;
+        int winc = w;
+#pragma unroll
+        for (int d = 1; d < 32; d <<= 1) {
+            const int y = __shfl_up_sync(0xffffffffu, winc, d);
+            if (lane >= d) winc += y;
+        }
+        warp_sums[lane] = winc - w;
+        if (lane == 31) *total = winc;
+    }
+    __syncthreads();
+    const int out = warp_sums[warp] + inc - v;
+    __syncthreads();
+    return out;
+}
+
+// Every CTA of a cooperative launch arrives; returns once `target` arrivals
+// have been counted (or false after kWaitLimitNs, recording the timeout).
+// Writes before the barrier are visible to every CTA after it.
+__device__ bool grid_barrier(unsigned *ctr, unsigned target, int *status, volatile int *s_ok) {
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();
+        atomicAdd(ctr, 1u);
+        int ok = 1;
+        const unsigned long long t0 = globaltimer();
+        while (*reinterpret_cast<volatile unsigned *>(ctr) < target) {
+            __nanosleep(64);
+            if (globaltimer() - t0 > kWaitLimitNs) {
+                if (status) atomicCAS(status, 0, kStatusTimeout);
+                ok = 0;
+                break;
+            }
+        }
+        __threadfence();
+        *s_ok = ok;
+    }
+    __syncthreads();
+    return *s_ok != 0;
+}
+
+template <int R, bool REORDER>
 __global__ void __launch_bounds__(kThreads, 1)
     router_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW1,
                   const RouterArgs args) {
@@ -201,7 +265,10 @@ __global__ void __launch_bounds__(kThreads, 1)
             if (++acc == 2) { acc = 0; acc_phase ^= 1u; }
 
             const int t = tile * BM + row;
-            if (t >= T) continue;
+            const bool valid = t < T;
+            if (!REORDER && !valid) continue;
+            // the tile's ballots, [tile][g][quad], for the fused reorder
+            uint32_t *bal = REORDER ? args.ws + 4 + static_cast<size_t>(tile) * ng * 4 : nullptr;
             uint8_t *mrow = args.mask + static_cast<size_t>(t) * ng;
             float *lrow = args.logits != nullptr ? args.logits + static_cast<size_t>(t) * 2 * ng : nullptr;
             for (int g0 = g_lo; g0 < g_hi; g0 += 4) {
@@ -231,11 +298,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (g >= g_hi) break;
                     const float r0 = acc8[2 * u], r1 = acc8[2 * u + 1];
                     const uint32_t m = r0 >= r1 ? 1u : 0u;  // argmax over (r0, r1): ties go to class 0
+                    if (REORDER) {
+                        const uint32_t b = __ballot_sync(0xffffffffu, valid && m != 0u);
+                        if (lane == 0) bal[g * 4 + quad] = b;
+                    }
+                    if (!valid) continue;
                     if (lrow != nullptr) *reinterpret_cast<float2 *>(lrow + 2 * g) = make_float2(r0, r1);
                     if (words) word |= m << (8 * u);
                     else mrow[g] = static_cast<uint8_t>(m);
                 }
-                if (words) *reinterpret_cast<uint32_t *>(mrow + g0) = word;
+                if (words && valid) *reinterpret_cast<uint32_t *>(mrow + g0) = word;
             }
         }
     }
@@ -246,13 +318,74 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
+    if constexpr (REORDER) {
+        __shared__ int warp_sums[32];
+        __shared__ int s_total;
+        __shared__ int s_ok;
+        unsigned *ctr = args.ws;
+        const uint32_t *bal = args.ws + 4;                                          // [tiles][ng][4]
+        int32_t *off = reinterpret_cast<int32_t *>(args.ws + 4 + static_cast<size_t>(n_tiles) * ng * 4);  // [tiles][ng]
+        const int tid = threadIdx.x;
+        // every CTA takes part in both barriers, also after a failure of its own
+        const bool ok1 = grid_barrier(ctr, gridDim.x, args.status, &s_ok) && !*s_abort;
+        // per group: exclusive scan of the tiles' active counts
+        for (int g = blockIdx.x; ok1 && g < ng; g += gridDim.x) {
+            int carry = 0;
+            for (int base = 0; base < n_tiles; base += kThreads) {
+                const int tile = base + tid;
+                int c = 0;
+                if (tile < n_tiles) {
+                    const uint4 b = __ldcg(reinterpret_cast<const uint4 *>(bal + (static_cast<size_t>(tile) * ng + g) * 4));
+                    c = __popc(b.x) + __popc(b.y) + __popc(b.z) + __popc(b.w);
+                }
+                const int ex = block_exclusive_scan(c, warp_sums, &s_total);
+                if (tile < n_tiles) off[static_cast<size_t>(tile) * ng + g] = carry + ex;
+                carry += s_total;
+                __syncthreads();
+            }
+            if (tid == 0) args.counts[g] = carry;
+        }
+        const bool ok2 = grid_barrier(ctr, 2u * gridDim.x, args.status, &s_ok);
+        if (!ok1 || !ok2) return;
+        // place this CTA's tokens: the stable partition of every group.  The
+        // tile's ballots and offsets and the counts are staged in the (now
+        // idle) pipeline stages first.
+        uint32_t *sb = reinterpret_cast<uint32_t *>(stages);  // [ng][4] ballots
+        int *so = reinterpret_cast<int *>(sb + ng * 4);       // [ng] tile offsets
+        int *sc = so + ng;                                    // [ng] counts
+        for (int i = tid; i < ng; i += kThreads) sc[i] = __ldcg(args.counts + i);
+        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+            for (int i = tid; i < ng; i += kThreads) {
+                reinterpret_cast<uint4 *>(sb)[i] =
+                    __ldcg(reinterpret_cast<const uint4 *>(bal + (static_cast<size_t>(tile) * ng + i) * 4));
+                so[i] = __ldcg(off + static_cast<size_t>(tile) * ng + i);
+            }
+            __syncthreads();
+            for (int idx = tid; idx < ng * BM; idx += kThreads) {
+                const int g = idx / BM, r = idx - g * BM;
+                const int t = tile * BM + r;
+                if (t >= T) continue;
+                const uint4 b = reinterpret_cast<const uint4 *>(sb)[g];
+                const int q = r >> 5, ln = r & 31;
+                const uint32_t wq = q == 0 ? b.x : q == 1 ? b.y : q == 2 ? b.z : b.w;
+                int before = __popc(wq & ((1u << ln) - 1u));
+                if (q > 0) before += __popc(b.x);
+                if (q > 1) before += __popc(b.y);
+                if (q > 2) before += __popc(b.z);
+                const int a_off = so[g];
+                const int pos = ((wq >> ln) & 1u) ? a_off + before : sc[g] + (tile * BM - a_off) + (r - before);
+                args.perm[static_cast<size_t>(g) * T + pos] = t;
+            }
+            __syncthreads();
+        }
+    }
 }
 
-template <int R>
+template <int R, bool REORDER = false>
 cudaError_t launch_t(const CUtensorMap &tmX, const CUtensorMap &tmW1, const RouterArgs &a, int num_sms,
                      cudaStream_t s) {
     using C = RouterCfg<R>;
-    auto kern = router_kernel<R>;
+    auto kern = router_kernel<R, REORDER>;
     const int w2_bytes = 2 * a.n_groups * R * 2;
     const int smem = C::smem_bytes(w2_bytes);
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
@@ -260,9 +393,18 @@ cudaError_t launch_t(const CUtensorMap &tmX, const CUtensorMap &tmW1, const Rout
     RouterArgs args = a;
     args.stages = C::stages(w2_bytes);
     const int tiles = (a.T + BM - 1) / BM;
-    const int grid = tiles < num_sms ? tiles : num_sms;
-    kern<<<grid, kThreads, smem, s>>>(tmX, tmW1, args);
-    return cudaGetLastError();
+    const int grid = tiles < num_sms ? tiles : num_sms;  // one CTA per SM at most: all resident
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = REORDER ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, kern, tmX, tmW1, args);
 }
 
 // ---------------------------------------------------------------------------
@@ -346,6 +488,19 @@ cudaError_t launch_router_decode(const uint16_t *X, const uint16_t *W1, const Ro
 bool router_supported(int r, int n_groups) {
     if (r != 16 && r != 32 && r != 64) return false;
     return n_groups >= 1 && 2 * n_groups * r * 2 <= kW2MaxBytes;
+}
+
+size_t route_reorder_workspace_bytes(int T, int n_groups) {
+    const size_t tiles = (static_cast<size_t>(T) + BM - 1) / BM;
+    return 16 + tiles * n_groups * (16 + 4);  // barrier counter, ballots, tile offsets
+}
+
+cudaError_t launch_route_reorder(const CUtensorMap &tmX, const CUtensorMap &tmW1, const RouterArgs &a,
+                                 int num_sms, cudaStream_t s) {
+    if (a.r == 16) return launch_t<16, true>(tmX, tmW1, a, num_sms, s);
+    if (a.r == 32) return launch_t<32, true>(tmX, tmW1, a, num_sms, s);
+    if (a.r == 64) return launch_t<64, true>(tmX, tmW1, a, num_sms, s);
+    return cudaErrorInvalidValue;
 }
 
 cudaError_t launch_router(const CUtensorMap &tmX, const CUtensorMap &tmW1, const RouterArgs &a,

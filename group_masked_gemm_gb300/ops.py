@@ -66,6 +66,8 @@ def lib():
                 L.wide_attn_decode_workspace_size.argtypes = [i, i, i, i]
                 L.wide_attn_decode_workspace_size.restype = sz
                 L.wide_attn_prefill.argtypes = [p, p, p, p, p, i, i, i, i, i, i, p, p]
+                L.wide_route_and_reorder_workspace_size.argtypes = [i, i]
+                L.wide_route_and_reorder_workspace_size.restype = sz
                 for fn in ("wide_reorder_masks", "wide_gemm_mn_gate_up", "wide_gemm_k_down",
                            "wide_proj_mn", "wide_proj_k", "wide_device_status",
                            "wide_gemm_k_decode_noalloc", "wide_router_masks",
@@ -142,8 +144,15 @@ def router_masks(X, W1, W2, mask=None, logits=False, stream=None):
     return (mask, lg) if logits else mask
 
 
-def route_and_reorder(X, W1, W2, mask=None, perm=None, counts=None, stream=None):
-    """Router then mask reordering: returns (mask, perm [ng, T], counts [ng])."""
+def route_and_reorder_workspace_size(T, n_groups) -> int:
+    return int(lib().wide_route_and_reorder_workspace_size(T, n_groups))
+
+
+def route_and_reorder(X, W1, W2, mask=None, perm=None, counts=None, ws=None, fused=True,
+                      stream=None):
+    """Router then mask reordering: returns (mask, perm [ng, T], counts [ng]).
+    With ``fused`` (and T > 16) both run as one kernel launch in a workspace
+    (``ws``, allocated here when not given); otherwise as two launches."""
     _need(X, torch.bfloat16, "X", 2)
     T, D = X.shape
     r = W1.shape[0]
@@ -152,9 +161,14 @@ def route_and_reorder(X, W1, W2, mask=None, perm=None, counts=None, stream=None)
     mask = torch.empty((T, ng), dtype=torch.uint8, device=dev) if mask is None else mask
     perm = torch.empty((ng, T), dtype=torch.int32, device=dev) if perm is None else perm
     counts = torch.empty((ng,), dtype=torch.int32, device=dev) if counts is None else counts
+    need = route_and_reorder_workspace_size(T, ng) if fused else 0
+    if need and ws is None:
+        ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+    if not fused:
+        ws = None
     _check("wide_route_and_reorder", lib().wide_route_and_reorder(
         _ptr(X), _ptr(W1), _ptr(W2), T, D, r, ng, _ptr(mask), _ptr(perm), _ptr(counts),
-        None, 0, _stream(stream)))
+        _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
     return mask, perm, counts
 
 

@@ -137,8 +137,9 @@ size_t wide_attn_decode_workspace_size(int B, int Hq, int d, int L_max);
  *   perm, counts : for every sequence b, wide_reorder_masks() of its mask
  *            mask[b] ([T, Hk]): perm [B, Hk, T] int32, counts [B, Hk] int32
  *   O      : bf16 [B, T, Hq, d] (every element written)
- * Scores and P V run on the warp-level tensor cores (bf16 in, fp32
- * accumulate; P rounded to bf16); the softmax is online in fp32.
+ * Scores and P V run on the tensor cores (tcgen05 with S and O in TMEM for
+ * d = 128, the warp-level instruction for d = 64; bf16 in, fp32 accumulate,
+ * P rounded to bf16); the softmax is online in fp32.
  * d in {64, 128} (else WIDE_ERR_UNSUPPORTED); B, Hq <= 65535.
  */
 wide_status_t wide_attn_prefill(const uint16_t *Q, const uint16_t *K, const uint16_t *V,
@@ -149,7 +150,16 @@ wide_status_t wide_attn_prefill(const uint16_t *Q, const uint16_t *K, const uint
  * The router followed by the mask reordering of that mask (Eq. 4-5 then
  * Eq. 7), both enqueued on `stream`: mask, perm and counts are ready for the
  * GEMM calls.  Arguments as for wide_router_masks and wide_reorder_masks.
+ *   ws : with at least wide_route_and_reorder_workspace_size(T, n_groups)
+ *        bytes (16-byte aligned; nonzero only for T > 16), the two run as
+ *        one cooperative kernel launch (after an 8-byte memset of the
+ *        workspace): each CTA routes its 128-token tiles, and after grid
+ *        barriers the CTAs scan the per-tile active counts and place their
+ *        own tokens.  With a smaller or NULL workspace, or T <= 16, the
+ *        router and the reorder kernel run one after the other.  Same
+ *        results either way (perm and counts bit-identical).
  */
+size_t wide_route_and_reorder_workspace_size(int T, int n_groups);
 wide_status_t wide_route_and_reorder(const uint16_t *X, const uint16_t *W1, const uint16_t *W2,
                                      int T, int d_model, int r, int n_groups, uint8_t *mask,
                                      int32_t *perm, int32_t *counts, void *ws, size_t ws_bytes,

@@ -66,6 +66,29 @@ def test_router_parity(T, D, r, ng):
     assert 0.2 < mask_ref.mean() < 0.8
 
 
+@pytest.mark.parametrize("T,D,r,ng", [(2000, 1024, 32, 56), (16384, 4096, 32, 112), (300, 512, 16, 13),
+                                      (129, 256, 64, 8), (40000, 512, 32, 112), (17, 1024, 32, 1024)])
+def test_route_and_reorder_fused_matches_two_launches(T, D, r, ng):
+    """The one-launch router + reorder (cooperative kernel, grid barriers) gives
+    the mask of the router alone and the oracle's reorder of it, bit for bit.
+    T = 40000 gives CTAs several tiles; ng = 13 and 1024 are not multiples of
+    4; T = 129 and 17 leave a partial tile."""
+    if 2 * ng * r * 2 > 64 * 1024:
+        r = 16
+    X, W1, W2 = _router_case(T, D, r, ng, seed=T + ng)
+    Xd, W1d, W2d = to_dev(X), to_dev(W1), to_dev(W2)
+    assert ops.route_and_reorder_workspace_size(T, ng) > 0
+    mask_f, perm_f, counts_f = ops.route_and_reorder(Xd, W1d, W2d)
+    mask_2, perm_2, counts_2 = ops.route_and_reorder(Xd, W1d, W2d, fused=False)
+    ops.device_status()
+    m = mask_f.cpu().numpy()
+    np.testing.assert_array_equal(m, mask_2.cpu().numpy())
+    perm_ref, counts_ref = oracle.reorder(m)
+    np.testing.assert_array_equal(counts_f.cpu().numpy(), counts_ref)
+    np.testing.assert_array_equal(perm_f.cpu().numpy(), perm_ref)
+    np.testing.assert_array_equal(perm_2.cpu().numpy(), perm_ref)
+
+
 def test_route_and_reorder_bit_exact():
     X, W1, W2 = _router_case(2000, 1024, 32, 56, seed=7)
     mask, perm, counts = ops.route_and_reorder(to_dev(X), to_dev(W1), to_dev(W2))
