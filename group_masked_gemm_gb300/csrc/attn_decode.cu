@@ -83,6 +83,9 @@ __global__ void __launch_bounds__(kThreads)
     float *ps = reinterpret_cast<float *>(smem + 2 * TILE);  // [kChunk][QPK]
     uint64_t *bar = reinterpret_cast<uint64_t *>(ps + kChunk * QPK);
 
+    // the combine kernel (a programmatic dependent) may be scheduled now; it
+    // waits for this grid before it reads the partials
+    griddep_launch_dependents();
     const int chunk = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
     const int L = min(max(a.lens[b], 0), a.L_max);  // lengths outside [0, L_max] are clamped
     const int j0 = chunk * kChunk;
@@ -224,6 +227,7 @@ __global__ void __launch_bounds__(kThreads)
 template <int D>
 __global__ void __launch_bounds__(kThreads)
     attn_combine_kernel(const AttnDecodeArgs a) {
+    griddep_wait();  // the chunk partials are the previous kernel's output
     __shared__ float wts[1024];  // per-chunk weights exp(m_c - M) / sum
     const int h = blockIdx.x, b = blockIdx.y;
     const int qpk = a.Hq / a.Hk, g = h / qpk;
@@ -273,8 +277,17 @@ cudaError_t launch_t(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnD
     if (e != cudaSuccess) return e;
     kp<<<dim3(a.n_chunks, a.Hk, a.B), kThreads, smem, s>>>(tmK, tmV, a);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
-    attn_combine_kernel<D><<<dim3(a.Hq, a.B), kThreads, 0, s>>>(a);
-    return cudaGetLastError();
+    // the combine overlaps the chunk kernel's tail (programmatic dependent launch)
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(a.Hq, a.B);
+    cfg.blockDim = dim3(kThreads);
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, attn_combine_kernel<D>, a);
 }
 
 template <int D>

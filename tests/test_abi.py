@@ -49,6 +49,12 @@ def test_host_only_entry_points(libwide):
     assert ws16 > 0 and ws16 % (16 * 4096 * 4) == 0
     libwide.wide_reorder_workspace_size.restype = ctypes.c_size_t
     assert libwide.wide_reorder_workspace_size(16384, 112) == 0
+    # one-launch router + reorder: barrier word, then per (128-token tile, group)
+    # four 32-bit ballots and one tile offset; none for decode (T <= 16)
+    libwide.wide_route_and_reorder_workspace_size.restype = ctypes.c_size_t
+    assert libwide.wide_route_and_reorder_workspace_size(16384, 112) == 16 + 128 * 112 * 20
+    assert libwide.wide_route_and_reorder_workspace_size(300, 13) == 16 + 3 * 13 * 20
+    assert libwide.wide_route_and_reorder_workspace_size(16, 112) == 0
 
 
 def test_argument_errors_are_reported_before_any_launch(libwide):
