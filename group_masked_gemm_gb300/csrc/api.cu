@@ -372,7 +372,10 @@ wide_status_t wide_route_and_reorder(const uint16_t *X, const uint16_t *W1, cons
         a.perm = perm;
         a.counts = counts;
         a.ws = static_cast<uint32_t *>(ws);
-        return from_cuda(wide::launch_route_reorder(tmX, tmW1, a, ctx.num_sms, s));
+        const cudaError_t e = wide::launch_route_reorder(tmX, tmW1, a, ctx.num_sms, s);
+        if (e != cudaErrorCooperativeLaunchTooLarge) return from_cuda(e);
+        // the grid could not be co-resident (e.g. a partitioned GPU): two launches
+        (void)cudaGetLastError();
     }
     wide_status_t st = wide_router_masks(X, W1, W2, T, d_model, r, n_groups, mask, nullptr, stream);
     if (st != WIDE_OK) return st;

@@ -155,9 +155,10 @@ wide_status_t wide_attn_prefill(const uint16_t *Q, const uint16_t *K, const uint
  *        one cooperative kernel launch (after an 8-byte memset of the
  *        workspace): each CTA routes its 128-token tiles, and after grid
  *        barriers the CTAs scan the per-tile active counts and place their
- *        own tokens.  With a smaller or NULL workspace, or T <= 16, the
- *        router and the reorder kernel run one after the other.  Same
- *        results either way (perm and counts bit-identical).
+ *        own tokens.  With a smaller or NULL workspace, or T <= 16, or when
+ *        the device cannot keep the whole grid resident, the router and the
+ *        reorder kernel run one after the other.  Same results either way
+ *        (perm and counts bit-identical).
  */
 size_t wide_route_and_reorder_workspace_size(int T, int n_groups);
 wide_status_t wide_route_and_reorder(const uint16_t *X, const uint16_t *W1, const uint16_t *W2,
