@@ -1,6 +1,7 @@
 // attn_prefill.cu -- routed causal prefill attention (WIDE, App. B
 // "Implementation of Attention", prefill, Algorithm 4; GQA-aligned routing
-// groups of Sec. 3.1 Eq. 2).
+// groups of Sec. 3.1 Eq. 2) on the warp-level tensor-core instruction, the
+// kernel for head dim 64 (head dim 128 runs on tcgen05, attn_prefill_tc.cu).
 //
 // Query head h of sequence b reads KV head g = h / (Hq/Hk), which is also its
 // routing group.  The stable partition of the group's mask column (perm,
