@@ -69,6 +69,15 @@ __device__ __forceinline__ uint32_t swz(int half, int r, int c) {
     return static_cast<uint32_t>((c >> 3) * half + r * 128 + (((c & 7) ^ (r & 7)) << 4));
 }
 
+// 2^x on the special-function unit, denormal results flushed to zero (the
+// PTX ex2.approx.ftz instruction, relative error about 2^-22: far below the
+// bf16 rounding of P that follows).
+__device__ __forceinline__ float ex2(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Shared-memory descriptor of an MN-major operand in the 128-byte swizzle:
 // 64-element rows of the contiguous (MN) dimension, one row per K index,
 // 8-row atoms 1024 B apart along K, the two 64-element MN halves `half` apart.
@@ -274,7 +283,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
             if (j == 0) {
                 m_run = m_new;
             } else if (__any_sync(0xffffffffu, m_new > m_run + kRescaleSlack)) {
-                alpha = exp2f(m_run - m_new);
+                alpha = ex2(m_run - m_new);
                 m_run = m_new;
                 rescale = true;
             }
@@ -283,7 +292,7 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
             float sum4[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
             for (int e = 0; e < BKV; ++e) {
-                v[e] = exp2f(fmaf(v[e], sl2, -m_run));  // exp2(score * log2(e) / sqrt(d) - max)
+                v[e] = ex2(fmaf(v[e], sl2, -m_run));  // exp2(score * log2(e) / sqrt(d) - max)
                 sum4[e & 3] += v[e];
             }
             const float sum = (sum4[0] + sum4[1]) + (sum4[2] + sum4[3]);
