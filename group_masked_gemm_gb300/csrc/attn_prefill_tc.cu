@@ -78,6 +78,13 @@ __device__ __forceinline__ float ex2(float x) {
     return y;
 }
 
+// max(a, b, c) in one instruction (the three-input form of PTX max.f32).
+__device__ __forceinline__ float max3(float a, float b, float c) {
+    float y;
+    asm("max.f32 %0, %1, %2, %3;" : "=f"(y) : "f"(a), "f"(b), "f"(c));
+    return y;
+}
+
 // Shared-memory descriptor of an MN-major operand in the 128-byte swizzle:
 // 64-element rows of the contiguous (MN) dimension, one row per K index,
 // 8-row atoms 1024 B apart along K, the two 64-element MN halves `half` apart.
@@ -264,17 +271,21 @@ __global__ void __launch_bounds__(kThreadsTc, 2)
             const int k0 = j * BKV;
             const bool cut = (a.causal && k0 + BKV - 1 > min_pos) || k0 + BKV > T;
             // raw scores; the cut ones become -inf, and the row maximum (the
-            // scale is positive) runs in 4 independent chains
-            float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+            // scale is positive) runs in 2 chains of three-input maxima
+            if (cut) {
 #pragma unroll
-            for (int e = 0; e < BKV; ++e) {
-                if (cut) {
+                for (int e = 0; e < BKV; ++e) {
                     const int kpos = k0 + e;
                     if (kpos >= T || (a.causal && kpos > qpos)) v[e] = -INFINITY;
                 }
-                mx4[e & 3] = fmaxf(mx4[e & 3], v[e]);
             }
-            const float mx = fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3])) * sl2;
+            float mxa = -INFINITY, mxb = -INFINITY;
+#pragma unroll
+            for (int e = 0; e < BKV; e += 4) {
+                mxa = max3(mxa, v[e], v[e + 1]);
+                mxb = max3(mxb, v[e + 2], v[e + 3]);
+            }
+            const float mx = fmaxf(mxa, mxb) * sl2;
             // the running maximum; a warp rescales when any of its rows grew by
             // more than the slack (then every lane moves to its new maximum)
             const float m_new = fmaxf(m_run, mx);
