@@ -81,6 +81,11 @@ constexpr int kMaxGroups = 1024;
 
 cudaError_t launch_reorder(const uint8_t *mask, int T, int n_groups, int32_t *perm,
                            int32_t *counts, cudaStream_t s);
+// Cooperative reorder with coalesced mask reads: ws holds
+// partition_workspace_bytes(T, n_groups) bytes, its first 16 zeroed.
+size_t reorder_coop_smem_bytes(int n_groups);
+cudaError_t launch_reorder_coop(const uint8_t *mask, int T, int n_groups, int32_t *perm, int32_t *counts,
+                                uint32_t *ws, int *status, int num_sms, cudaStream_t s);
 
 // tmB0/tmB1: tiled maps over the weights [n_out, K] (box 64 x bn, 128-B swizzle)
 cudaError_t launch_gemm_mn(MNMode mode, int bn, const CUtensorMap &tmB0, const CUtensorMap &tmB1,

@@ -6,18 +6,28 @@
 // active counts gives every run its output positions: active tokens go to
 // the prefix in ascending order, inactive tokens after counts[g] in
 // ascending order.  Columns longer than 32 * blockDim tokens are processed in
-// chunks after a counting pass.
+// chunks after a counting pass.  This kernel reads each column at a stride of
+// n_groups bytes.
+//
+// With a workspace, reorder_coop_kernel does the same partition from
+// coalesced reads of the mask rows instead: a cooperative grid stages each
+// 128-token tile's mask rows in shared memory, ballots every group over the
+// tile's four 32-token warps, and finishes with the scan and placement of
+// partition.cuh (grid barriers between the phases).
 #include "common.cuh"
 #include "internal.h"
+#include "partition.cuh"
 
 namespace wide {
 namespace {
 
 constexpr int kThreads = 1024;
 constexpr int kRun = 32;  // tokens per thread per chunk (one bit each)
+constexpr int kCoopThreads = 256;
+constexpr int kGroupChunk = 128;  // mask columns staged per pass
 
 // Exclusive scan of v over the block; *total receives the block sum.
-__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
+__device__ __forceinline__ int column_exclusive_scan(int v, int *warp_sums, int *total) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     int inc = v;
 #pragma unroll
@@ -60,7 +70,7 @@ __global__ void __launch_bounds__(kThreads)
         int c = 0;
         for (long long t = tid; t < T; t += kThreads)
             c += mask[static_cast<size_t>(t) * n_groups + g] != 0;
-        block_exclusive_scan(c, warp_sums, &s_total);
+        column_exclusive_scan(c, warp_sums, &s_total);
         __syncthreads();
         total = s_total;
     }
@@ -81,7 +91,7 @@ __global__ void __launch_bounds__(kThreads)
             }
         }
         const int n_act = __popc(bits);
-        const int a_off = block_exclusive_scan(n_act, warp_sums, &s_total);
+        const int a_off = column_exclusive_scan(n_act, warp_sums, &s_total);
         __syncthreads();
         const int chunk_active = s_total;
         if (total < 0) total = chunk_active;  // single chunk: column total known now
@@ -99,7 +109,74 @@ __global__ void __launch_bounds__(kThreads)
     if (tid == 0) counts[g] = total;
 }
 
+// Cooperative stable partition: ballots of each tile (coalesced row reads
+// staged in shared memory), then partition_scan / partition_place.
+__global__ void __launch_bounds__(kCoopThreads)
+    reorder_coop_kernel(const uint8_t *__restrict__ mask, int T, int ng, int32_t *__restrict__ perm,
+                        int32_t *__restrict__ counts, uint32_t *ws, int *status) {
+    extern __shared__ __align__(16) uint8_t smem[];  // [128][kGroupChunk] mask bytes, then scratch
+    __shared__ int warp_sums[32];
+    __shared__ int s_total;
+    __shared__ int s_ok;
+    const int n_tiles = (T + kPartTile - 1) / kPartTile;
+    const PartitionWs w = partition_ws(ws, n_tiles, ng);
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int q = warp & 3;  // this warp's 32-token quarter of the tile
+    for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
+        const int t0 = tile * kPartTile;
+        for (int g0 = 0; g0 < ng; g0 += kGroupChunk) {
+            const int gc = min(kGroupChunk, ng - g0);
+            for (int i = threadIdx.x; i < kPartTile * gc; i += kCoopThreads) {
+                const int r = i / gc, c = i - r * gc;
+                const int t = t0 + r;
+                smem[r * kGroupChunk + c] = t < T ? mask[static_cast<size_t>(t) * ng + g0 + c] : 0;
+            }
+            __syncthreads();
+            // warps 0-3 and 4-7 take alternate groups; each ballots its quarter
+            for (int c = warp >> 2; c < gc; c += kCoopThreads / 128) {
+                const uint32_t b = __ballot_sync(0xffffffffu, smem[(q * 32 + lane) * kGroupChunk + c] != 0);
+                if (lane == 0) w.bal[(static_cast<size_t>(tile) * ng + g0 + c) * 4 + q] = b;
+            }
+            __syncthreads();
+        }
+    }
+    const bool ok1 = grid_barrier(w.ctr, gridDim.x, status, &s_ok);
+    if (ok1) partition_scan(w, n_tiles, ng, counts, warp_sums, &s_total);
+    const bool ok2 = grid_barrier(w.ctr, 2u * gridDim.x, status, &s_ok);
+    if (!ok1 || !ok2) return;
+    partition_place(w, n_tiles, ng, T, counts, perm, smem + kPartTile * kGroupChunk);
+}
+
 }  // namespace
+
+size_t reorder_coop_smem_bytes(int n_groups) {
+    return static_cast<size_t>(kPartTile) * kGroupChunk + static_cast<size_t>(n_groups) * 24;
+}
+
+cudaError_t launch_reorder_coop(const uint8_t *mask, int T, int n_groups, int32_t *perm, int32_t *counts,
+                                uint32_t *ws, int *status, int num_sms, cudaStream_t s) {
+    const size_t smem = reorder_coop_smem_bytes(n_groups);
+    cudaError_t e = cudaFuncSetAttribute(reorder_coop_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    int per_sm = 0;
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, reorder_coop_kernel, kCoopThreads, smem);
+    if (e != cudaSuccess) return e;
+    if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+    const int tiles = (T + kPartTile - 1) / kPartTile;
+    const int grid = tiles < per_sm * num_sms ? tiles : per_sm * num_sms;  // every CTA resident
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeCooperative;
+    attr[0].val.cooperative = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(grid);
+    cfg.blockDim = dim3(kCoopThreads);
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, reorder_coop_kernel, mask, T, n_groups, perm, counts, ws, status);
+}
 
 cudaError_t launch_reorder(const uint8_t *mask, int T, int n_groups, int32_t *perm,
                            int32_t *counts, cudaStream_t s) {

@@ -27,6 +27,7 @@
 // the barriers are bounded waits on a counter in the workspace.
 #include "common.cuh"
 #include "internal.h"
+#include "partition.cuh"
 
 namespace wide {
 namespace {
@@ -60,60 +61,6 @@ struct RouterCfg {
         return 1024 + stages(w2_bytes) * STAGE_BYTES + ((w2_bytes + 15) & ~15) + BAR_BYTES;
     }
 };
-
-// Exclusive scan of v over the block; *total receives the block sum.
-__device__ __forceinline__ int block_exclusive_scan(int v, int *warp_sums, int *total) {
-    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    int inc = v;
-#pragma unroll
-    for (int d = 1; d < 32; d <<= 1) {
-        const int y = __shfl_up_sync(0xffffffffu, inc, d);
-        if (lane >= d) inc += y;
-    }
-    if (lane == 31) warp_sums[warp] = inc;
-    __syncthreads();
-    if (warp == 0) {
-        const int nw = blockDim.x >> 5;
-        const int w = lane < nw ? warp_sums[lane] : 0;
-        int winc = w;
-#pragma unroll
-        for (int d = 1; d < 32; d <<= 1) {
-            const int y = __shfl_up_sync(0xffffffffu, winc, d);
-            if (lane >= d) winc += y;
-        }
-        warp_sums[lane] = winc - w;
-        if (lane == 31) *total = winc;
-    }
-    __syncthreads();
-    const int out = warp_sums[warp] + inc - v;
-    __syncthreads();
-    return out;
-}
-
-// Every CTA of a cooperative launch arrives; returns once `target` arrivals
-// have been counted (or false after kWaitLimitNs, recording the timeout).
-// Writes before the barrier are visible to every CTA after it.
-__device__ bool grid_barrier(unsigned *ctr, unsigned target, int *status, volatile int *s_ok) {
-    __syncthreads();
-    if (threadIdx.x == 0) {
-        __threadfence();
-        atomicAdd(ctr, 1u);
-        int ok = 1;
-        const unsigned long long t0 = globaltimer();
-        while (*reinterpret_cast<volatile unsigned *>(ctr) < target) {
-            __nanosleep(64);
-            if (globaltimer() - t0 > kWaitLimitNs) {
-                if (status) atomicCAS(status, 0, kStatusTimeout);
-                ok = 0;
-                break;
-            }
-        }
-        __threadfence();
-        *s_ok = ok;
-    }
-    __syncthreads();
-    return *s_ok != 0;
-}
 
 template <int R, bool REORDER>
 __global__ void __launch_bounds__(kThreads, 1)
@@ -268,7 +215,8 @@ __global__ void __launch_bounds__(kThreads, 1)
             const bool valid = t < T;
             if (!REORDER && !valid) continue;
             // the tile's ballots, [tile][g][quad], for the fused reorder
-            uint32_t *bal = REORDER ? args.ws + 4 + static_cast<size_t>(tile) * ng * 4 : nullptr;
+            uint32_t *bal = REORDER ? partition_ws(args.ws, n_tiles, ng).bal + static_cast<size_t>(tile) * ng * 4
+                                    : nullptr;
             uint8_t *mrow = args.mask + static_cast<size_t>(t) * ng;
             float *lrow = args.logits != nullptr ? args.logits + static_cast<size_t>(t) * 2 * ng : nullptr;
             for (int g0 = g_lo; g0 < g_hi; g0 += 4) {
@@ -319,65 +267,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_dealloc(tmem_base, C::TMEM_COLS);
     }
     if constexpr (REORDER) {
+        static_assert(BM == kPartTile, "one ballot tile per router tile");
         __shared__ int warp_sums[32];
         __shared__ int s_total;
         __shared__ int s_ok;
-        unsigned *ctr = args.ws;
-        const uint32_t *bal = args.ws + 4;                                          // [tiles][ng][4]
-        int32_t *off = reinterpret_cast<int32_t *>(args.ws + 4 + static_cast<size_t>(n_tiles) * ng * 4);  // [tiles][ng]
-        const int tid = threadIdx.x;
+        const PartitionWs w = partition_ws(args.ws, n_tiles, ng);
         // every CTA takes part in both barriers, also after a failure of its own
-        const bool ok1 = grid_barrier(ctr, gridDim.x, args.status, &s_ok) && !*s_abort;
-        // per group: exclusive scan of the tiles' active counts
-        for (int g = blockIdx.x; ok1 && g < ng; g += gridDim.x) {
-            int carry = 0;
-            for (int base = 0; base < n_tiles; base += kThreads) {
-                const int tile = base + tid;
-                int c = 0;
-                if (tile < n_tiles) {
-                    const uint4 b = __ldcg(reinterpret_cast<const uint4 *>(bal + (static_cast<size_t>(tile) * ng + g) * 4));
-                    c = __popc(b.x) + __popc(b.y) + __popc(b.z) + __popc(b.w);
-                }
-                const int ex = block_exclusive_scan(c, warp_sums, &s_total);
-                if (tile < n_tiles) off[static_cast<size_t>(tile) * ng + g] = carry + ex;
-                carry += s_total;
-                __syncthreads();
-            }
-            if (tid == 0) args.counts[g] = carry;
-        }
-        const bool ok2 = grid_barrier(ctr, 2u * gridDim.x, args.status, &s_ok);
+        const bool ok1 = grid_barrier(w.ctr, gridDim.x, args.status, &s_ok) && !*s_abort;
+        if (ok1) partition_scan(w, n_tiles, ng, args.counts, warp_sums, &s_total);
+        const bool ok2 = grid_barrier(w.ctr, 2u * gridDim.x, args.status, &s_ok);
         if (!ok1 || !ok2) return;
-        // place this CTA's tokens: the stable partition of every group.  The
-        // tile's ballots and offsets and the counts are staged in the (now
-        // idle) pipeline stages first.
-        uint32_t *sb = reinterpret_cast<uint32_t *>(stages);  // [ng][4] ballots
-        int *so = reinterpret_cast<int *>(sb + ng * 4);       // [ng] tile offsets
-        int *sc = so + ng;                                    // [ng] counts
-        for (int i = tid; i < ng; i += kThreads) sc[i] = __ldcg(args.counts + i);
-        for (int tile = blockIdx.x; tile < n_tiles; tile += gridDim.x) {
-            for (int i = tid; i < ng; i += kThreads) {
-                reinterpret_cast<uint4 *>(sb)[i] =
-                    __ldcg(reinterpret_cast<const uint4 *>(bal + (static_cast<size_t>(tile) * ng + i) * 4));
-                so[i] = __ldcg(off + static_cast<size_t>(tile) * ng + i);
-            }
-            __syncthreads();
-            for (int idx = tid; idx < ng * BM; idx += kThreads) {
-                const int g = idx / BM, r = idx - g * BM;
-                const int t = tile * BM + r;
-                if (t >= T) continue;
-                const uint4 b = reinterpret_cast<const uint4 *>(sb)[g];
-                const int q = r >> 5, ln = r & 31;
-                const uint32_t wq = q == 0 ? b.x : q == 1 ? b.y : q == 2 ? b.z : b.w;
-                int before = __popc(wq & ((1u << ln) - 1u));
-                if (q > 0) before += __popc(b.x);
-                if (q > 1) before += __popc(b.y);
-                if (q > 2) before += __popc(b.z);
-                const int a_off = so[g];
-                const int pos = ((wq >> ln) & 1u) ? a_off + before : sc[g] + (tile * BM - a_off) + (r - before);
-                args.perm[static_cast<size_t>(g) * T + pos] = t;
-            }
-            __syncthreads();
-        }
+        // the tile's ballots and offsets are staged in the (now idle) pipeline stages
+        partition_place(w, n_tiles, ng, T, args.counts, args.perm, stages);
     }
 }
 
@@ -490,10 +391,7 @@ bool router_supported(int r, int n_groups) {
     return n_groups >= 1 && 2 * n_groups * r * 2 <= kW2MaxBytes;
 }
 
-size_t route_reorder_workspace_bytes(int T, int n_groups) {
-    const size_t tiles = (static_cast<size_t>(T) + BM - 1) / BM;
-    return 16 + tiles * n_groups * (16 + 4);  // barrier counter, ballots, tile offsets
-}
+size_t route_reorder_workspace_bytes(int T, int n_groups) { return partition_workspace_bytes(T, n_groups); }
 
 cudaError_t launch_route_reorder(const CUtensorMap &tmX, const CUtensorMap &tmW1, const RouterArgs &a,
                                  int num_sms, cudaStream_t s) {

@@ -113,16 +113,33 @@ def device_status(stream=None) -> None:
     _check("wide_device_status", lib().wide_device_status(_stream(stream)))
 
 
-def reorder_masks(mask, perm=None, counts=None, stream=None):
-    """Eq. 7 stable SortDesc per routing column -> (perm [ng, T], counts [ng])."""
+def reorder_workspace_size(T, n_groups) -> int:
+    return int(lib().wide_reorder_workspace_size(T, n_groups))
+
+
+def reorder_masks(mask, perm=None, counts=None, ws=None, coop=None, stream=None):
+    """Eq. 7 stable SortDesc per routing column -> (perm [ng, T], counts [ng]).
+    coop=None follows the library's choice (wide_reorder_workspace_size);
+    True forces the one-launch cooperative kernel, False one block per column."""
     _need(mask, torch.uint8, "mask", 2)
     T, ng = mask.shape
     if perm is None:
         perm = torch.empty((ng, T), dtype=torch.int32, device=mask.device)
     if counts is None:
         counts = torch.empty((ng,), dtype=torch.int32, device=mask.device)
+    if coop is None:
+        need = reorder_workspace_size(T, ng)
+    elif coop:
+        need = 16 + 20 * ((T + 127) // 128) * ng
+    else:
+        need = 0
+    if need and ws is None:
+        ws = torch.empty((need,), dtype=torch.uint8, device=mask.device)
+    if coop is False or need == 0:
+        ws = None
     _check("wide_reorder_masks", lib().wide_reorder_masks(
-        _ptr(mask), T, ng, _ptr(perm), _ptr(counts), None, 0, _stream(stream)))
+        _ptr(mask), T, ng, _ptr(perm), _ptr(counts), _ptr(ws), 0 if ws is None else ws.numel(),
+        _stream(stream)))
     return perm, counts
 
 

@@ -75,7 +75,15 @@ int wide_num_sms(void);
  *   mask   : uint8 [T, n_groups] row-major (device)
  *   perm   : int32 [n_groups, T] group-major (device, written)
  *   counts : int32 [n_groups]    (device, written)
- *   ws     : unused, may be NULL (wide_reorder_workspace_size() returns 0)
+ *   ws     : optional.  With 16 + 20 * ceil(T/128) * n_groups bytes (16-byte
+ *            aligned), the partition runs as one cooperative kernel launch
+ *            (after an 8-byte memset of the workspace) that reads the mask
+ *            rows coalesced and ballots each group over 32-token warps;
+ *            otherwise (ws NULL or smaller, or a grid that cannot be
+ *            resident) one block per column walks its column.  Same result
+ *            either way.  wide_reorder_workspace_size() returns that size
+ *            where the cooperative launch measured faster (T >= 49152, or
+ *            T >= 16384 with n_groups <= 32), else 0.
  * Bit-exact and deterministic.  T <= 2^31 - 1, 1 <= n_groups <= 65535.
  */
 wide_status_t wide_reorder_masks(const uint8_t *mask, int T, int n_groups,

@@ -48,7 +48,12 @@ def test_host_only_entry_points(libwide):
     ws16 = libwide.wide_gemm_k_workspace_size(16, 14336, 4096, 128)
     assert ws16 > 0 and ws16 % (16 * 4096 * 4) == 0
     libwide.wide_reorder_workspace_size.restype = ctypes.c_size_t
+    # the cooperative reorder (barrier word, ballots and tile offsets per (tile,
+    # group)) is requested where it measured faster: few groups or long columns
     assert libwide.wide_reorder_workspace_size(16384, 112) == 0
+    assert libwide.wide_reorder_workspace_size(16384, 8) == 16 + 128 * 8 * 20
+    assert libwide.wide_reorder_workspace_size(4096, 8) == 0
+    assert libwide.wide_reorder_workspace_size(65536, 112) == 16 + 512 * 112 * 20
     # one-launch router + reorder: barrier word, then per (128-token tile, group)
     # four 32-bit ballots and one tile offset; none for decode (T <= 16)
     libwide.wide_route_and_reorder_workspace_size.restype = ctypes.c_size_t

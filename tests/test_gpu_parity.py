@@ -34,14 +34,15 @@ def _bits_dev(rng, shape, scale=1.0):
 
 # ----------------------------------------------------------------- reorder ---
 
+@pytest.mark.parametrize("coop", [True, False])  # one cooperative launch / one block per column
 @pytest.mark.parametrize("T,ng,keep,seed", [
     (1, 1, 0.5, 0), (7, 3, 0.5, 1), (64, 8, 0.5, 2), (300, 28, 0.3, 3),
     (4096, 64, 0.5, 4), (16384, 112, 0.5, 5), (40000, 5, 0.5, 6), (129, 224, 0.1, 7),
-    (1000, 3, 0.0, 8), (1000, 3, 1.0, 9), (65537, 2, 0.7, 10)])
-def test_reorder_bit_exact(T, ng, keep, seed):
+    (1000, 3, 0.0, 8), (1000, 3, 1.0, 9), (65537, 2, 0.7, 10), (200000, 3, 0.5, 11)])
+def test_reorder_bit_exact(T, ng, keep, seed, coop):
     mask = syn.random_mask(T, ng, keep, seed)
     mask[::7] *= 255  # any nonzero byte is active
-    perm, counts = ops.reorder_masks(mask_dev(mask))
+    perm, counts = ops.reorder_masks(mask_dev(mask), coop=coop)
     torch.cuda.synchronize()
     p_ref, c_ref = oracle.reorder(mask)
     assert np.array_equal(counts.cpu().numpy(), c_ref)
