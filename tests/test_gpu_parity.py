@@ -96,7 +96,11 @@ def test_proj_mn_parity(T, K, N, G, keep):
     # G = 512 (o_proj-sized groups), ragged T, all-active and all-inactive
     (300, 2048, 512, 512, 1.0), (300, 2048, 512, 512, 0.0), (1029, 4096, 768, 512, 0.34),
     # short batches: the groups are split over CTAs with fp32 partials
-    (33, 14336, 4096, 128, 0.5), (200, 2048, 1024, 128, 0.05)])
+    (33, 14336, 4096, 128, 0.5), (200, 2048, 1024, 128, 0.05),
+    # wide outputs (256-column tiles over grids that fill the SMs), ragged T
+    (2048, 1024, 4096, 128, 0.5), (2000, 2048, 4096, 128, 0.3), (1900, 1024, 4096, 256, 0.5),
+    (1280, 4096, 4096, 512, 0.34), (1536, 1024, 4096, 128, 1.0), (1536, 1024, 4096, 128, 0.0),
+    (2304, 512, 8192, 64, 0.02)])
 def test_gemm_k_parity(T, K, N, G, keep):
     rng = np.random.default_rng(T * 3 + G)
     A = _bits_dev(rng, (T, K))
