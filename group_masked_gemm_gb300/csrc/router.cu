@@ -9,9 +9,9 @@
 // persistent CTA owns 128 token rows: TMA streams X tiles (the M = 128 side)
 // and W1 tiles (the N = r side) into a pipeline as deep as shared memory
 // allows next to W2 (up to 10 stages), one thread issues tcgen05.mma with
-// the fp32 accumulator in TMEM (double-buffered across tiles), and eight
-// epilogue warps -- two per TMEM lane quadrant, one token row per thread,
-// each taking half of the groups -- read z from TMEM, form the logits with
+// the fp32 accumulator in TMEM (double-buffered across tiles), and sixteen
+// epilogue warps (eight for r = 64) -- four (two) per TMEM lane quadrant, one
+// token row per thread, each taking a share of the groups -- read z from TMEM, form the logits with
 // fp32 FMAs in ascending j against W2 held in shared memory (four groups at
 // a time, eight independent chains), and write the mask row (and optionally
 // the logits).
@@ -34,8 +34,10 @@ namespace {
 
 constexpr int BM = 128;
 constexpr int BK = 64;
-constexpr int kEpiWarps = 8;
-constexpr int kThreads = 32 * (2 + kEpiWarps);  // warp 0 TMA, warp 1 MMA + TMEM, 2..9 epilogue
+// warp 0 TMA, warp 1 MMA + TMEM, then the epilogue warps: four per TMEM lane
+// quadrant for r <= 32, two for r = 64 (whose z row needs twice the registers)
+template <int R> __host__ __device__ constexpr int epi_warps() { return R >= 64 ? 8 : 16; }
+template <int R> __host__ __device__ constexpr int router_threads() { return 32 * (2 + epi_warps<R>()); }
 constexpr int kMaxStages = 10;
 constexpr int kW2MaxBytes = 64 * 1024;
 constexpr int kSmemBudget = 225 * 1024;
@@ -63,7 +65,7 @@ struct RouterCfg {
 };
 
 template <int R, bool REORDER>
-__global__ void __launch_bounds__(kThreads, 1)
+__global__ void __launch_bounds__(router_threads<R>(), 1)
     router_kernel(const __grid_constant__ CUtensorMap tmX, const __grid_constant__ CUtensorMap tmW1,
                   const RouterArgs args) {
     using C = RouterCfg<R>;
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         for (int b = 0; b < 2; ++b) {
             mbar_init(&tfull[b], 1);
-            mbar_init(&tempty[b], kEpiWarps);
+            mbar_init(&tempty[b], epi_warps<R>());
         }
         mbar_init(final_bar, 1);
         *s_abort = 0;
@@ -114,7 +116,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const int n16 = w2_bytes / 16;
         const uint4 *src = reinterpret_cast<const uint4 *>(args.W2);
         uint4 *dst = reinterpret_cast<uint4 *>(w2s);
-        for (int i = threadIdx.x; i < n16; i += kThreads) dst[i] = src[i];
+        for (int i = threadIdx.x; i < n16; i += router_threads<R>()) dst[i] = src[i];
     }
     tc_fence_before();
     __syncthreads();
@@ -181,14 +183,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     } else {
         // ===================== epilogue (warps 2..9) =====================
         const int quad = warp & 3;      // TMEM lanes 32*quad .. 32*quad+31
-        const int half = (warp - 2) >> 2;  // which half of the groups
+        constexpr int kParts = epi_warps<R>() / 4;
+        const int part = (warp - 2) >> 2;  // which share of the groups
         const int row = quad * 32 + lane;
         int acc = 0;
         uint32_t acc_phase = 0;
         const bool words = (ng & 3) == 0;  // mask rows start on 4-byte boundaries
-        const int g_split = ((ng + 7) / 8) * 4;  // a multiple of 4: word stores never straddle halves
-        const int g_lo = half == 0 ? 0 : min(ng, g_split);
-        const int g_hi = half == 0 ? min(ng, g_split) : ng;
+        // shares of a multiple of 4 groups: word stores never straddle two shares
+        const int g_chunk = ((ng + 4 * kParts - 1) / (4 * kParts)) * 4;
+        const int g_lo = min(ng, part * g_chunk);
+        const int g_hi = part == kParts - 1 ? ng : min(ng, (part + 1) * g_chunk);
         for (int tile = blockIdx.x; tile < n_tiles && !*s_abort; tile += gridDim.x) {
             int ok = 1;
             if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, args.status);
@@ -300,7 +304,7 @@ cudaError_t launch_t(const CUtensorMap &tmX, const CUtensorMap &tmW1, const Rout
     attr[0].val.cooperative = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(grid);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(router_threads<R>());
     cfg.dynamicSmemBytes = smem;
     cfg.stream = s;
     cfg.attrs = attr;
