@@ -131,6 +131,16 @@ wide_status_t check_mn(const void *X, const void *W0, const void *W1, const void
     return WIDE_OK;
 }
 
+// Workspace a GEMM-K call cannot run without: fp32 partial sums of a split
+// reduction (decode, and prefill grids smaller than the SMs).  The prefill
+// tail split's workspace is optional (wide_gemm_k_workspace_size reports it).
+size_t gemm_k_required_ws(int T, int K, int N, int G) {
+    if (T < 1 || G <= 0 || K < G || K % G) return 0;
+    if (T > kDecodeMaxT) return wide::gemm_k_split_workspace_bytes(T, K, N, G, sizing_sms());
+    return decode_k_on_gemm_k(N) ? wide::gemm_k_decode_workspace_bytes(T, K, N, G, sizing_sms())
+                                 : wide::decode_k_workspace_bytes(T, K, N, G);
+}
+
 wide_status_t check_k(const void *A, const void *W, const void *mask, int T, int K, int N, int G,
                       const void *out, const void *ws, size_t ws_bytes) {
     if (!good_ptr(A) || !good_ptr(W) || !good_ptr(mask) || !good_ptr(out))
@@ -139,7 +149,7 @@ wide_status_t check_k(const void *A, const void *W, const void *mask, int T, int
     if (!good_group(G) && !whole_width_group(G, K)) return bad_group_status(G);
     if (K % G) return WIDE_ERR_INVALID_ARG;
     if (K / G > wide::gemm_k_max_groups()) return WIDE_ERR_UNSUPPORTED;
-    const size_t need = wide_gemm_k_workspace_size(T, K, N, G);
+    const size_t need = gemm_k_required_ws(T, K, N, G);
     if (need > 0 && (ws == nullptr || ws_bytes < need)) return WIDE_ERR_WORKSPACE;
     if (need > 0 && !aligned16(ws)) return WIDE_ERR_INVALID_ARG;
     return WIDE_OK;
@@ -184,7 +194,7 @@ wide_status_t run_mn(wide::MNMode mode, const uint16_t *X, const uint16_t *W0,
 }
 
 wide_status_t run_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask, int T, int K,
-                    int N, int G, uint16_t *out, void *ws, void *stream) {
+                    int N, int G, uint16_t *out, void *ws, size_t ws_bytes, void *stream) {
     DeviceCtx ctx;
     wide_status_t st = device_ctx(&ctx);
     if (st != WIDE_OK) return st;
@@ -217,6 +227,9 @@ wide_status_t run_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask, i
     if ((st = encode_bf16_2d(&tmA, A, T, K, 128)) != WIDE_OK) return st;
     if ((st = encode_bf16_2d(&tmB, W, N, K, bn)) != WIDE_OK) return st;
     wide::KArgs a{mask, out, T, K, N, G, ctx.status};
+    const size_t tail = wide::gemm_k_tail_workspace_bytes(T, K, N, G, ctx.num_sms);
+    if (tail > 0 && ws != nullptr && ws_bytes >= tail && aligned16(ws))
+        return from_cuda(wide::launch_gemm_k_tail(bn, tmA, tmB, a, static_cast<float *>(ws), ctx.num_sms, s));
     return from_cuda(wide::launch_gemm_k(bn, tmA, tmB, a, ctx.num_sms, s));
 }
 
@@ -428,15 +441,13 @@ wide_status_t wide_proj_mn(const uint16_t *X, const uint16_t *W, const uint8_t *
 }
 
 size_t wide_gemm_k_workspace_size(int T, int K, int N, int G) {
-    // Large prefill reduces in TMEM and needs none; decode, and prefill too
-    // small to fill the SMs, sum fp32 partials of the split reduction dimension.
-    if (T < 1 || G <= 0 || K < G || K % G) return 0;
-    if (T > kDecodeMaxT) {
-        const int sms = sizing_sms();
-        return wide::gemm_k_split_workspace_bytes(T, K, N, G, sms);
-    }
-    return decode_k_on_gemm_k(N) ? wide::gemm_k_decode_workspace_bytes(T, K, N, G, sizing_sms())
-                                 : wide::decode_k_workspace_bytes(T, K, N, G);
+    // Decode, and prefill too small to fill the SMs, sum fp32 partials of the
+    // split reduction dimension (required).  Large prefill reduces in TMEM; when
+    // its last wave of output tiles would leave half of the SMs idle, an
+    // optional workspace lets that wave's tiles be split (the tail split).
+    const size_t need = gemm_k_required_ws(T, K, N, G);
+    if (need > 0 || T <= kDecodeMaxT || T < 1 || G <= 0 || K < G || K % G) return need;
+    return wide::gemm_k_tail_workspace_bytes(T, K, N, G, sizing_sms());
 }
 
 wide_status_t wide_gemm_k_down(const uint16_t *H, const uint16_t *W_down, const uint8_t *mask,
@@ -447,7 +458,7 @@ wide_status_t wide_gemm_k_down(const uint16_t *H, const uint16_t *W_down, const 
     (void)counts;
     wide_status_t st = check_k(H, W_down, mask, T, d_ffn, d_model, G, Y, ws, ws_bytes);
     if (st != WIDE_OK) return st;
-    return run_k(H, W_down, mask, T, d_ffn, d_model, G, Y, ws, stream);
+    return run_k(H, W_down, mask, T, d_ffn, d_model, G, Y, ws, ws_bytes, stream);
 }
 
 wide_status_t wide_proj_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask,
@@ -457,7 +468,7 @@ wide_status_t wide_proj_k(const uint16_t *A, const uint16_t *W, const uint8_t *m
     (void)counts;
     wide_status_t st = check_k(A, W, mask, T, K, N, G, Y, ws, ws_bytes);
     if (st != WIDE_OK) return st;
-    return run_k(A, W, mask, T, K, N, G, Y, ws, stream);
+    return run_k(A, W, mask, T, K, N, G, Y, ws, ws_bytes, stream);
 }
 
 wide_status_t wide_device_status(void *stream) {

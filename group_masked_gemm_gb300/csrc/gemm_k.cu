@@ -186,6 +186,45 @@ __device__ __forceinline__ int build_tile_masks(const uint8_t *__restrict__ mask
     return n_live;
 }
 
+// Work unit i of the persistent grid: output tile (mt, nt), share sp of nsp
+// equal shares of the tile's live groups, and its tail-partial slot (-1: the
+// unit writes Y, or the [splits][T][N] partial planes of a split launch).
+struct KUnit {
+    int mt, nt, sp, nsp, slot;
+};
+
+__device__ __forceinline__ KUnit k_unit(int i, int n_tiles, const KArgs &a) {
+    KUnit u;
+    if (a.n_direct < 0) {
+        u.mt = i / (n_tiles * a.splits);
+        const int rem = i - u.mt * n_tiles * a.splits;
+        u.sp = rem / n_tiles;
+        u.nt = rem - u.sp * n_tiles;
+        u.nsp = a.splits;
+        u.slot = -1;
+    } else if (i < a.n_direct) {
+        u.mt = i / n_tiles;
+        u.nt = i - u.mt * n_tiles;
+        u.sp = 0;
+        u.nsp = 1;
+        u.slot = -1;
+    } else {
+        const int j = i - a.n_direct;
+        const int item = a.n_direct + j / a.tail_splits;
+        u.mt = item / n_tiles;
+        u.nt = item - u.mt * n_tiles;
+        u.sp = j - (j / a.tail_splits) * a.tail_splits;
+        u.nsp = a.tail_splits;
+        u.slot = j;
+    }
+    return u;
+}
+
+__host__ __device__ __forceinline__ int k_units(int m_tiles, int n_tiles, const KArgs &a) {
+    return a.n_direct < 0 ? m_tiles * n_tiles * a.splits
+                          : a.n_direct + (m_tiles * n_tiles - a.n_direct) * a.tail_splits;
+}
+
 template <int BN, int AR>
 __global__ void __launch_bounds__(kThreads, 1)
     gemm_k_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmB,
@@ -212,8 +251,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const int ng = args.K / args.G;
     const int m_tiles = (T + BM - 1) / BM;
     const int n_tiles = args.N / BN;
-    const int splits = args.splits;
-    const int n_items = m_tiles * n_tiles * splits;
+    const int n_items = k_units(m_tiles, n_tiles, args);
     const int kb_per_group = args.G / BK;
     const bool partial_out = args.partial != nullptr;
     const uint32_t stage_bytes = static_cast<uint32_t>(args.a_rows * BK * 2 + C::B_BYTES);
@@ -277,9 +315,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int b = 0;
         uint32_t bphase = 0;
         for (int i = blockIdx.x; i < n_items && !*s_abort; i += gridDim.x) {
-            const int mt = i / (n_tiles * splits);
-            const int sp = (i - mt * n_tiles * splits) / n_tiles;
-            const int m0 = mt * BM;
+            const KUnit u = k_unit(i, n_tiles, args);
+            const int m0 = u.mt * BM;
             int ok = 1;
             if (lane == 0) ok = mbar_wait(&mempty[b], bphase ^ 1u, args.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -292,8 +329,8 @@ __global__ void __launch_bounds__(kThreads, 1)
                 n_all = build_decode_masks(args.mask, T, ng, mbuf.lanes, mbuf.live);
             }
             // equal contiguous shares of the tile's live groups, one per split
-            const int per = (n_all + splits - 1) / splits;
-            const int first = min(n_all, sp * per);
+            const int per = (n_all + u.nsp - 1) / u.nsp;
+            const int first = min(n_all, u.sp * per);
             const int n_live = min(n_all, first + per) - first;
             if (lane == 0) {
                 *mbuf.n_live = n_live;
@@ -312,8 +349,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         int b = 0;
         uint32_t bphase = 0;
         for (int i = blockIdx.x; i < n_items && !*s_abort; i += gridDim.x) {
-            const int mt = i / (n_tiles * splits);
-            const int nt = (i - mt * n_tiles * splits) % n_tiles;
+            const KUnit u = k_unit(i, n_tiles, args);
+            const int mt = u.mt, nt = u.nt;
             int ok = 1;
             if (lane == 0) ok = mbar_wait(&mfull[b], bphase, args.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -404,10 +441,9 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
         for (int q = 0; q < 32; ++q) z[q] = 0u;
         for (int i = blockIdx.x; i < n_items && !*s_abort; i += gridDim.x) {
-            const int mt = i / (n_tiles * splits);
-            const int rem = i - mt * n_tiles * splits;
-            const int sp = rem / n_tiles, nt = rem - sp * n_tiles;
-            const int t = mt * BM + row;
+            const KUnit u = k_unit(i, n_tiles, args);
+            const int sp = u.sp, nt = u.nt;
+            const int t = u.mt * BM + row;
             int ok = 1;
             if (lane == 0) ok = mbar_wait(&tfull[acc], acc_phase, args.status);
             ok = __shfl_sync(0xffffffffu, ok, 0);
@@ -422,7 +458,17 @@ __global__ void __launch_bounds__(kThreads, 1)
                 tmem_ld32(taddr + cb, yr);
                 tmem_ld_wait();
                 tmem_st32(taddr + cb, z);
-                if (partial_out) {
+                if (u.slot >= 0) {
+                    // fp32 partial of this tail share, compact [slot][BM][BN]
+                    if (t < T) {
+                        float *pdst = args.tail_partial + (static_cast<size_t>(u.slot) * BM + row) * BN + cb;
+#pragma unroll
+                        for (int q = 0; q < 8; ++q)
+                            *reinterpret_cast<float4 *>(pdst + 4 * q) =
+                                make_float4(__uint_as_float(yr[4 * q]), __uint_as_float(yr[4 * q + 1]),
+                                            __uint_as_float(yr[4 * q + 2]), __uint_as_float(yr[4 * q + 3]));
+                    }
+                } else if (partial_out) {
                     // fp32 partial of this split; rows past T (and the lanes
                     // the token box did not fill) were masked off and are not stored
                     if (t < T) {
@@ -467,7 +513,7 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM_BYTES);
     if (e != cudaSuccess) return e;
     const int m_tiles = (a.T + BM - 1) / BM;
-    const int items = m_tiles * (a.N / BN) * a.splits;
+    const int items = k_units(m_tiles, a.N / BN, a);
     const int grid = items < num_sms ? items : num_sms;
     cudaLaunchAttribute pdl[1];
     pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
@@ -482,6 +528,64 @@ cudaError_t launch_t(const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs
     return cudaLaunchKernelEx(&cfg, kern, tmA, tmB, a);
 }
 
+
+// Tail finalize: Y of tail item j (item n_direct + j) is the sum of its nsp
+// shares' fp32 partials, added in share order; 8 columns per thread.
+constexpr int kFinThreads = 256;
+
+__global__ void __launch_bounds__(kFinThreads)
+    gemm_k_tail_finalize_kernel(const float *__restrict__ tp, int n_direct, int tail_items, int nsp,
+                                int n_tiles, int bn, int T, int N, uint16_t *__restrict__ out) {
+    griddep_wait();  // the partials are the GEMM-K kernel's output
+    const int per_item = BM * (bn / 8);
+    const long long idx = static_cast<long long>(blockIdx.x) * kFinThreads + threadIdx.x;
+    if (idx >= static_cast<long long>(tail_items) * per_item) return;
+    const int j = static_cast<int>(idx / per_item);
+    const int rem = static_cast<int>(idx - static_cast<long long>(j) * per_item);
+    const int r = rem / (bn / 8), c = (rem - r * (bn / 8)) * 8;
+    const int item = n_direct + j;
+    const int mt = item / n_tiles, nt = item - mt * n_tiles;
+    const int t = mt * BM + r;
+    if (t >= T) return;
+    float acc[8];
+#pragma unroll
+    for (int e = 0; e < 8; ++e) acc[e] = 0.f;
+    for (int sp = 0; sp < nsp; ++sp) {
+        const float4 *src = reinterpret_cast<const float4 *>(
+            tp + (static_cast<size_t>(j * nsp + sp) * BM + r) * bn + c);
+        const float4 v0 = src[0], v1 = src[1];
+        acc[0] += v0.x; acc[1] += v0.y; acc[2] += v0.z; acc[3] += v0.w;
+        acc[4] += v1.x; acc[5] += v1.y; acc[6] += v1.z; acc[7] += v1.w;
+    }
+    st_global_v4(out + static_cast<size_t>(t) * N + nt * bn + c, pack_bf16x2(acc[0], acc[1]),
+                 pack_bf16x2(acc[2], acc[3]), pack_bf16x2(acc[4], acc[5]), pack_bf16x2(acc[6], acc[7]));
+}
+
+// The tail split: with `items` output tiles on num_sms persistent CTAs, the
+// last wave holds items % num_sms tiles.  When that wave would leave at least
+// half of the SMs idle, its tiles are cut into s equal shares of their live
+// groups (s <= 4, s tiles' shares at most one wave), so the wave takes about
+// 1/s of a tile's time.  n_direct < 0: no split.
+struct KTailPlan {
+    int n_direct, splits;
+    size_t bytes;
+};
+
+KTailPlan tail_plan(int T, int K, int N, int G, int num_sms) {
+    const KTailPlan none{-1, 1, 0};
+    const int bn = N % 256 == 0 ? 256 : N % 128 == 0 ? 128 : 64;
+    if (T <= 16 || N % bn != 0 || num_sms < 2) return none;
+    const long long items = static_cast<long long>((T + BM - 1) / BM) * (N / bn);
+    if (items < num_sms || items > (1ll << 30)) return none;
+    const int tail = static_cast<int>(items % num_sms);
+    if (tail == 0 || 2 * tail > num_sms) return none;
+    int s = num_sms / tail;
+    s = s > 4 ? 4 : s;
+    s = s > K / G ? K / G : s;
+    if (s < 2) return none;
+    return KTailPlan{static_cast<int>(items - tail), s,
+                     static_cast<size_t>(tail) * s * BM * bn * sizeof(float)};
+}
 
 }  // namespace
 
@@ -567,6 +671,41 @@ cudaError_t launch_gemm_k_decode(const CUtensorMap &tmA, const CUtensorMap &tmB,
                                                  : launch_t<128, 16>(tmA, tmB, a, num_sms, s, true);
     if (e != cudaSuccess) return e;
     return launch_decode_k_finalize(ws, a.splits, a.T * a.N, a.out, s);
+}
+
+size_t gemm_k_tail_workspace_bytes(int T, int K, int N, int G, int num_sms) {
+    return tail_plan(T, K, N, G, num_sms).bytes;
+}
+
+cudaError_t launch_gemm_k_tail(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a0,
+                               float *ws, int num_sms, cudaStream_t s) {
+    const KTailPlan p = tail_plan(a0.T, a0.K, a0.N, a0.G, num_sms);
+    const int expect_bn = a0.N % 256 == 0 ? 256 : a0.N % 128 == 0 ? 128 : 64;
+    if (p.n_direct < 0 || bn != expect_bn || ws == nullptr) return cudaErrorInvalidValue;
+    KArgs a = a0;
+    a.splits = 1;
+    a.partial = nullptr;
+    a.n_direct = p.n_direct;
+    a.tail_splits = p.splits;
+    a.tail_partial = ws;
+    cudaError_t e = launch_gemm_k(bn, tmA, tmB, a, num_sms, s);
+    if (e != cudaSuccess) return e;
+    const int n_tiles = a.N / bn;
+    const int tail_items = ((a.T + BM - 1) / BM) * n_tiles - p.n_direct;
+    const long long threads = static_cast<long long>(tail_items) * BM * (bn / 8);
+    // a programmatic dependent of the GEMM-K kernel: its launch overlaps that
+    // kernel's tail, and griddep_wait orders its reads after the partials
+    cudaLaunchAttribute pdl[1];
+    pdl[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    pdl[0].val.programmaticStreamSerializationAllowed = 1;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>((threads + kFinThreads - 1) / kFinThreads));
+    cfg.blockDim = dim3(kFinThreads);
+    cfg.stream = s;
+    cfg.attrs = pdl;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, gemm_k_tail_finalize_kernel, static_cast<const float *>(ws), p.n_direct,
+                              tail_items, p.splits, n_tiles, bn, a.T, a.N, a.out);
 }
 
 cudaError_t launch_gemm_k(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a,

@@ -31,6 +31,13 @@ struct KArgs {
     float *partial = nullptr;
     int splits = 1;
     int a_rows = 128;  // rows of the token-row TMA box (<= 128)
+    // Prefill tail split (n_direct >= 0): the first n_direct items write Y
+    // directly; each later item is cut into tail_splits equal shares of its
+    // live groups, share s of the j-th such item writing fp32 partial sums
+    // to tail_partial[j * tail_splits + s][BM][BN].
+    int n_direct = -1;
+    int tail_splits = 1;
+    float *tail_partial = nullptr;
 };
 
 struct RouterArgs {
@@ -93,6 +100,11 @@ cudaError_t launch_gemm_mn(MNMode mode, int bn, const CUtensorMap &tmB0, const C
 
 // tmA: tiled map over the token-row operand [T, K] (box 64 x 128)
 // tmB: tiled map over the weights [N, K] (box 64 x bn)
+// Prefill tail split: workspace bytes (0 = the split does not apply) and the
+// launch (the GEMM-K kernel, then a finalize that adds the shares in order).
+size_t gemm_k_tail_workspace_bytes(int T, int K, int N, int G, int num_sms);
+cudaError_t launch_gemm_k_tail(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB, const KArgs &a,
+                               float *ws, int num_sms, cudaStream_t s);
 cudaError_t launch_gemm_k(int bn, const CUtensorMap &tmA, const CUtensorMap &tmB,
                           const KArgs &a, int num_sms, cudaStream_t s);
 

@@ -11,6 +11,7 @@ CPU fallback.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 import threading
@@ -86,6 +87,17 @@ def _stream(stream=None):
     return ctypes.c_void_p(s.cuda_stream)
 
 
+def _scratch(nbytes, device, stream=None):
+    """A workspace allocated here for one call.  When the call runs on another
+    stream than torch's current one, the tensor is recorded as in use there, so
+    the caching allocator does not hand its memory out again before the kernels
+    queued on that stream have finished with it."""
+    t = torch.empty((nbytes,), dtype=torch.uint8, device=device)
+    if stream is not None and stream != torch.cuda.current_stream(t.device):
+        t.record_stream(stream)
+    return t
+
+
 def _check(fn, status):
     if status != 0:
         raise WideError(fn, status)
@@ -134,7 +146,7 @@ def reorder_masks(mask, perm=None, counts=None, ws=None, coop=None, stream=None)
     else:
         need = 0
     if need and ws is None:
-        ws = torch.empty((need,), dtype=torch.uint8, device=mask.device)
+        ws = _scratch(need, mask.device, stream)
     if coop is False or need == 0:
         ws = None
     _check("wide_reorder_masks", lib().wide_reorder_masks(
@@ -180,7 +192,7 @@ def route_and_reorder(X, W1, W2, mask=None, perm=None, counts=None, ws=None, fus
     counts = torch.empty((ng,), dtype=torch.int32, device=dev) if counts is None else counts
     need = route_and_reorder_workspace_size(T, ng) if fused else 0
     if need and ws is None:
-        ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+        ws = _scratch(need, dev, stream)
     if not fused:
         ws = None
     _check("wide_route_and_reorder", lib().wide_route_and_reorder(
@@ -204,7 +216,7 @@ def attn_decode(Q, K, V, lens, mask, out=None, ws=None, stream=None):
         out = torch.empty((B, Hq, d), dtype=torch.bfloat16, device=Q.device)
     need = lib().wide_attn_decode_workspace_size(B, Hq, d, L_max)
     if ws is None:
-        ws = torch.empty((max(need, 16),), dtype=torch.uint8, device=Q.device)
+        ws = _scratch(max(need, 16), Q.device, stream)
     _check("wide_attn_decode", lib().wide_attn_decode(
         _ptr(Q), _ptr(K), _ptr(V), _ptr(lens), _ptr(mask), B, Hq, Hk, d, L_max, _ptr(out),
         _ptr(ws), ws.numel(), _stream(stream)))
@@ -222,13 +234,15 @@ def attn_prefill(Q, K, V, mask, causal=True, perm=None, counts=None, out=None, s
     B, T, Hq, d = Q.shape
     Hk = K.shape[1]
     if perm is None or counts is None:
-        perm = torch.empty((B, Hk, T), dtype=torch.int32, device=Q.device)
-        counts = torch.empty((B, Hk), dtype=torch.int32, device=Q.device)
-        for b in range(B):
-            # per-sequence slices need not be 16-byte aligned: reorder into fresh buffers
-            pb, cb = reorder_masks(mask[b].clone(), stream=stream)
-            perm[b].copy_(pb)
-            counts[b].copy_(cb)
+        # the copies below are torch ops: run them on the call's stream too
+        with torch.cuda.stream(stream) if stream is not None else contextlib.nullcontext():
+            perm = torch.empty((B, Hk, T), dtype=torch.int32, device=Q.device)
+            counts = torch.empty((B, Hk), dtype=torch.int32, device=Q.device)
+            for b in range(B):
+                # per-sequence slices need not be 16-byte aligned: reorder into fresh buffers
+                pb, cb = reorder_masks(mask[b].clone(), stream=stream)
+                perm[b].copy_(pb)
+                counts[b].copy_(cb)
     if out is None:
         out = torch.empty((B, T, Hq, d), dtype=torch.bfloat16, device=Q.device)
     _check("wide_attn_prefill", lib().wide_attn_prefill(
@@ -268,7 +282,7 @@ def gemm_k_down(H, W_down, mask, perm, counts, G, out=None, ws=None, stream=None
         out = torch.empty((T, D), dtype=torch.bfloat16, device=H.device)
     need = gemm_k_workspace_size(T, F, D, G)
     if need and ws is None:
-        ws = torch.empty((need,), dtype=torch.uint8, device=H.device)
+        ws = _scratch(need, H.device, stream)
     _check("wide_gemm_k_down", lib().wide_gemm_k_down(
         _ptr(H), _ptr(W_down), _ptr(mask), _ptr(perm), _ptr(counts), T, F, D, G,
         _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))
@@ -301,7 +315,7 @@ def proj_k(A, W, mask, perm, counts, G, out=None, ws=None, stream=None):
         out = torch.empty((T, N), dtype=torch.bfloat16, device=A.device)
     need = gemm_k_workspace_size(T, K, N, G)
     if need and ws is None:
-        ws = torch.empty((need,), dtype=torch.uint8, device=A.device)
+        ws = _scratch(need, A.device, stream)
     _check("wide_proj_k", lib().wide_proj_k(
         _ptr(A), _ptr(W), _ptr(mask), _ptr(perm), _ptr(counts), T, K, N, G,
         _ptr(out), _ptr(ws), 0 if ws is None else ws.numel(), _stream(stream)))

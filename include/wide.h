@@ -200,12 +200,18 @@ wide_status_t wide_gemm_mn_gate_up(const uint16_t *X, const uint16_t *W_gate,
  *   W_down : bf16 [d_model, d_ffn]
  *   mask   : uint8 [T, d_ffn/G]; perm/counts as above (may be NULL)
  *   Y      : bf16 [T, d_model] (written)
- *   ws     : device workspace of at least
- *            wide_gemm_k_workspace_size(T, d_ffn, d_model, G) bytes
- *            (may be NULL when that size is 0)
+ *   ws     : device workspace (16-byte aligned) of
+ *            wide_gemm_k_workspace_size(T, d_ffn, d_model, G) bytes.  For
+ *            decode and for batches too short to fill the GPU it is
+ *            required (WIDE_ERR_WORKSPACE without it).  For larger batches it
+ *            is optional: with it, the output tiles of a last wave that would
+ *            leave at least half of the SMs idle are cut into 2-4 equal
+ *            shares of their live groups (fp32 partials, added in order by
+ *            a second kernel); with ws NULL or smaller, every tile is
+ *            reduced whole.  NULL is accepted when the size is 0.
  * fp32 accumulation in ascending group order (when the groups are split over
- * CTAs -- decode, and batches too short to fill the GPU -- ascending within
- * each split, then the splits in order); deterministic.
+ * CTAs -- decode, short batches, the tail tiles above -- ascending within
+ * each share, then the shares in order); deterministic for a given device.
  */
 wide_status_t wide_gemm_k_down(const uint16_t *H, const uint16_t *W_down,
                                const uint8_t *mask, const int32_t *perm,
@@ -235,9 +241,11 @@ wide_status_t wide_proj_k(const uint16_t *A, const uint16_t *W,
                           const int32_t *counts, int T, int K, int N, int G,
                           uint16_t *Y, void *ws, size_t ws_bytes, void *stream);
 
-/* Workspace bytes a GEMM-K call needs for these sizes on the current device
- * (0 = none): fp32 partial sums when the groups are split over CTAs (T <= 16,
- * or a batch whose output-tile grid would leave SMs idle). */
+/* Workspace bytes a GEMM-K call takes for these sizes on the current device
+ * (0 = none): fp32 partial sums when the groups are split over CTAs -- T <= 16,
+ * a batch whose output-tile grid would leave SMs idle (both required), or the
+ * tiles of a mostly idle last wave of a larger batch (optional, see
+ * wide_gemm_k_down). */
 size_t wide_gemm_k_workspace_size(int T, int K, int N, int G);
 
 /*

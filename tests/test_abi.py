@@ -43,7 +43,10 @@ def test_host_only_entry_points(libwide):
     assert libwide.wide_status_string(99) == b"WIDE_ERR_UNKNOWN"
     assert libwide.wide_version() >= 10000
     libwide.wide_gemm_k_workspace_size.restype = ctypes.c_size_t
-    assert libwide.wide_gemm_k_workspace_size(16384, 14336, 4096, 128) == 0  # prefill: TMEM
+    # prefill reduces in TMEM; the optional workspace splits the tiles of a last
+    # wave that is at most half full: 2048 tiles on 152 SMs leave 72, cut in 2
+    assert libwide.wide_gemm_k_workspace_size(16384, 14336, 4096, 128) == 72 * 2 * 128 * 256 * 4
+    assert libwide.wide_gemm_k_workspace_size(2048, 1024, 4096, 128) == 0  # last wave 104 of 152
     # decode: fp32 partial sums of the split reduction dimension, [splits, T, N]
     ws16 = libwide.wide_gemm_k_workspace_size(16, 14336, 4096, 128)
     assert ws16 > 0 and ws16 % (16 * 4096 * 4) == 0

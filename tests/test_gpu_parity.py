@@ -121,6 +121,30 @@ def test_gemm_k_parity(T, K, N, G, keep):
     assert (Yg[mask.sum(1) == 0] == 0).all()
 
 
+@pytest.mark.parametrize("T,K,N,G,keep", [
+    # last waves of 8 (ragged last token tile), 40 and 8 tiles: shares of 4, 3, 4
+    (1200, 2048, 4096, 128, 0.5), (1536, 1024, 4096, 128, 0.3), (1280, 4096, 4096, 512, 0.34)])
+def test_gemm_k_tail_split(T, K, N, G, keep):
+    """Tiles of a mostly idle last wave split into shares of their live groups
+    (with the optional workspace) and reduced whole (without it): both match
+    the oracle."""
+    rng = np.random.default_rng(T + K + G)
+    A = _bits_dev(rng, (T, K))
+    W = _bits_dev(rng, (N, K), 0.02)
+    mask = (rng.random((T, K // G)) < keep).astype(np.uint8)
+    m = mask_dev(mask)
+    perm, counts = ops.reorder_masks(m)
+    assert ops.gemm_k_workspace_size(T, K, N, G) > 0  # the split applies on this device
+    ref = oracle.proj_k(A, W, mask, G)
+    for ws in (None, torch.empty((16,), dtype=torch.uint8, device="cuda")):
+        Y = _nan_like((T, N))
+        ops.gemm_k_down(to_dev(A), to_dev(W), m, perm, counts, G, out=Y, ws=ws)
+        ops.device_status()
+        Yg = to_f64(Y)
+        assert not np.isnan(Yg).any()
+        assert_close(Yg, ref, "gemm_k tail" if ws is None else "gemm_k whole")
+
+
 def test_proj_k_matches_gemm_k_down():
     rng = np.random.default_rng(42)
     T, K, N, G = 333, 4096, 512, 512
