@@ -19,9 +19,10 @@
 //     chunk softmax in fp32, then O = P V with P rounded to bf16.  Each
 //     head's chunk maximum m, sum l = sum exp(s - m) and o = sum exp(s - m) v
 //     go to the workspace.
-//   attn_combine: one CTA per (query head, sequence) merges the chunks in
-//     order (rescaling by exp(m_c - max m)) and writes bf16 O, or zeros for
-//     an inactive group or an empty cache.
+//   attn_combine: one CTA per (query head, sequence) merges the chunks
+//     (rescaling by exp(m_c - max m); contiguous chunk ranges summed in
+//     parallel, then added in order) and writes bf16 O, or zeros for an
+//     inactive group or an empty cache.
 #include <cmath>
 
 #include "common.cuh"
@@ -224,47 +225,110 @@ __global__ void __launch_bounds__(kThreads)
     }
 }
 
+// Block-wide reductions of the combine (fixed shuffle and warp order, so the
+// result does not depend on timing).  `red` holds one float per warp.
+constexpr int kCombThreads = 512;
+
+__device__ __forceinline__ float comb_block_max(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float w = threadIdx.x < kCombThreads / 32 ? red[threadIdx.x] : -INFINITY;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) w = fmaxf(w, __shfl_xor_sync(0xffffffffu, w, o));
+        if (threadIdx.x == 0) red[kCombThreads / 32] = w;
+    }
+    __syncthreads();
+    return red[kCombThreads / 32];
+}
+
+__device__ __forceinline__ float comb_block_sum(float v, float *red) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    __syncthreads();  // red may still be read by comb_block_max's callers
+    if ((threadIdx.x & 31) == 0) red[threadIdx.x >> 5] = v;
+    __syncthreads();
+    if (threadIdx.x < 32) {
+        float w = threadIdx.x < kCombThreads / 32 ? red[threadIdx.x] : 0.f;
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) w += __shfl_xor_sync(0xffffffffu, w, o);
+        if (threadIdx.x == 0) red[kCombThreads / 32] = w;
+    }
+    __syncthreads();
+    return red[kCombThreads / 32];
+}
+
+// One CTA per (query head, sequence) merges the chunk partials: M = max_c m_c,
+// w_c = exp(m_c - M), O = sum_c w_c o_c / sum_c w_c l_c.  The chunks' (m, l)
+// pairs are read by one thread each, and the weighted sum of the o_c rows is
+// cut into kCombThreads / D contiguous chunk ranges, each summed by D threads
+// with sixteen loads in flight; the ranges' sums are then added in order.
 template <int D>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kCombThreads)
     attn_combine_kernel(const AttnDecodeArgs a) {
+    static_assert(kCombThreads % D == 0, "whole parts of D threads");
+    constexpr int kParts = kCombThreads / D;
     griddep_wait();  // the chunk partials are the previous kernel's output
-    __shared__ float wts[1024];  // per-chunk weights exp(m_c - M) / sum
+    __shared__ float wts[1024];  // per-chunk weights exp(m_c - M)
+    __shared__ float red[kCombThreads / 32 + 1];
+    __shared__ float part[kCombThreads];  // [kParts][D] sums of the chunk ranges
     const int h = blockIdx.x, b = blockIdx.y;
     const int qpk = a.Hq / a.Hk, g = h / qpk;
     const int L = min(max(a.lens[b], 0), a.L_max);
     const bool active = a.mask[static_cast<size_t>(b) * a.Hk + g] != 0 && L > 0;
     uint16_t *orow = a.O + (static_cast<size_t>(b) * a.Hq + h) * D;
     if (!active) {
-        for (int e = threadIdx.x; e < D; e += kThreads) orow[e] = 0;
+        for (int e = threadIdx.x; e < D; e += kCombThreads) orow[e] = 0;
         return;
     }
-    const int n_valid = (L + kChunk - 1) / kChunk;
+    const int n_valid = (L + kChunk - 1) / kChunk;  // <= 1022 (L_max checked on the host)
     const size_t base = (static_cast<size_t>(b) * a.Hq + h) * a.n_chunks;
-    // maximum and normaliser over the chunks (one warp, chunks in ascending order)
-    if (threadIdx.x < 32) {
-        float M = -INFINITY;
-        for (int c = threadIdx.x; c < n_valid; c += 32) M = fmaxf(M, a.ws_ml[2 * (base + c)]);
+    // (m, l) of chunks tid and tid + kCombThreads
+    float m_c[2], l_c[2];
+    float mloc = -INFINITY;
 #pragma unroll
-        for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-        float wsum = 0.f;
-        for (int c0 = 0; c0 < n_valid; c0 += 32) {
-            const int c = c0 + threadIdx.x;
-            const float w = c < n_valid ? expf(a.ws_ml[2 * (base + c)] - M) : 0.f;
-            if (c < n_valid) wts[c % 1024] = w;
-            float t = c < n_valid ? w * a.ws_ml[2 * (base + c) + 1] : 0.f;
-#pragma unroll
-            for (int o = 16; o > 0; o >>= 1) t += __shfl_xor_sync(0xffffffffu, t, o);
-            wsum += t;
-        }
-        if (threadIdx.x == 0) wts[1023] = 1.f / wsum;  // n_valid <= 1022 (L_max checked on the host)
+    for (int k = 0; k < 2; ++k) {
+        const int c = threadIdx.x + k * kCombThreads;
+        m_c[k] = c < n_valid ? a.ws_ml[2 * (base + c)] : -INFINITY;
+        l_c[k] = c < n_valid ? a.ws_ml[2 * (base + c) + 1] : 0.f;
+        mloc = fmaxf(mloc, m_c[k]);
     }
+    const float M = comb_block_max(mloc, red);
+    float t = 0.f;
+#pragma unroll
+    for (int k = 0; k < 2; ++k) {
+        const int c = threadIdx.x + k * kCombThreads;
+        if (c < n_valid) {
+            const float w = expf(m_c[k] - M);
+            wts[c] = w;
+            t += w * l_c[k];
+        }
+    }
+    const float inv = 1.f / comb_block_sum(t, red);  // also publishes wts
+    // weighted sum of the o rows over this thread's chunk range
+    const int p = threadIdx.x / D, e = threadIdx.x - p * D;
+    const int per = (n_valid + kParts - 1) / kParts;
+    const int c0 = min(n_valid, p * per), c1 = min(n_valid, c0 + per);
+    const float *src = a.ws_o + (base + c0) * D + e;
+    float o = 0.f;
+    int c = c0;
+    for (; c + 16 <= c1; c += 16, src += 16 * D) {
+        float v[16];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) v[j] = src[j * D];
+#pragma unroll
+        for (int j = 0; j < 16; ++j) o = fmaf(v[j], wts[c + j], o);
+    }
+    for (; c < c1; ++c, src += D) o = fmaf(*src, wts[c], o);
+    part[threadIdx.x] = o;
     __syncthreads();
-    const float inv = wts[1023];
-    for (int e = threadIdx.x; e < D; e += kThreads) {
-        float o = 0.f;
-#pragma unroll 8
-        for (int c = 0; c < n_valid; ++c) o = fmaf(a.ws_o[(base + c) * D + e], wts[c], o);
-        orow[e] = f32_to_bf16(o * inv);
+    if (threadIdx.x < D) {
+        float sum = 0.f;
+#pragma unroll
+        for (int q = 0; q < kParts; ++q) sum += part[q * D + threadIdx.x];
+        orow[threadIdx.x] = f32_to_bf16(sum * inv);
     }
 }
 
@@ -283,7 +347,7 @@ cudaError_t launch_t(const CUtensorMap &tmK, const CUtensorMap &tmV, const AttnD
     pdl[0].val.programmaticStreamSerializationAllowed = 1;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(a.Hq, a.B);
-    cfg.blockDim = dim3(kThreads);
+    cfg.blockDim = dim3(kCombThreads);
     cfg.stream = s;
     cfg.attrs = pdl;
     cfg.numAttrs = 1;
