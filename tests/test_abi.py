@@ -47,6 +47,17 @@ def test_host_only_entry_points(libwide):
     # wave that is at most half full: 2048 tiles on 152 SMs leave 72, cut in 2
     assert libwide.wide_gemm_k_workspace_size(16384, 14336, 4096, 128) == 72 * 2 * 128 * 256 * 4
     assert libwide.wide_gemm_k_workspace_size(2048, 1024, 4096, 128) == 0  # last wave 104 of 152
+    tile = 128 * 256 * 4  # one fp32 share of a 128-token x 256-column tile
+    # 10 token tiles x 16 = 160 tiles: a last wave of 8, cut into min(4, 152 // 8) = 4 shares
+    assert libwide.wide_gemm_k_workspace_size(1200, 2048, 4096, 128) == 8 * 4 * tile
+    assert libwide.wide_gemm_k_workspace_size(1280, 4096, 4096, 512) == 8 * 4 * tile
+    # 192 tiles: a last wave of 40, 152 // 40 = 3 shares
+    assert libwide.wide_gemm_k_workspace_size(1536, 1024, 4096, 128) == 40 * 3 * tile
+    # a single group cannot be shared out
+    assert libwide.wide_gemm_k_workspace_size(1200, 128, 4096, 128) == 0
+    # fewer tiles than SMs: the required split workspace [splits, T, N], as before
+    ws_short = libwide.wide_gemm_k_workspace_size(1000, 1024, 768, 128)
+    assert ws_short > 0 and ws_short % (1000 * 768 * 4) == 0
     # decode: fp32 partial sums of the split reduction dimension, [splits, T, N]
     ws16 = libwide.wide_gemm_k_workspace_size(16, 14336, 4096, 128)
     assert ws16 > 0 and ws16 % (16 * 4096 * 4) == 0
