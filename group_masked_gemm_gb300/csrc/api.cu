@@ -238,11 +238,12 @@ wide_status_t run_k(const uint16_t *A, const uint16_t *W, const uint8_t *mask, i
 // The cooperative reorder costs about 13 us whatever the size (the workspace
 // memset and two grid barriers); one block per column grows with the column
 // and leaves SMs idle when groups are few.  Measured on GB300 (us, coop vs
-// column): 8 groups 13.9 vs 23.2 at T = 16384 but 13.6 vs 10.4 at T = 4096;
-// 32 groups 20.0 vs 23.0 at T = 16384; 64 groups 29.5 vs 23.6 at T = 16384;
-// 112 groups 52.5 vs 41.6 at T = 32768 and 62.8 vs 81.0 at T = 49152.
+// column): 8 groups 13.8 vs 17.1 at T = 16384 and 14.1 vs 26.9 at T = 32768,
+// but 13.5 vs 9.0 at T = 4096; 32 groups 20.2 vs 17.1 at T = 16384; 112
+// groups 52.2 vs 27.3 at T = 32768, 62.4 vs 62.3 at T = 49152 and 75.0 vs
+// 80.0 at T = 65536.
 static bool reorder_prefers_coop(int T, int n_groups) {
-    return T >= 49152 || (T >= 16384 && n_groups <= 32);
+    return T >= 65536 || (T >= 16384 && n_groups <= 16);
 }
 
 static bool reorder_coop_fits(int n_groups) { return wide::reorder_coop_smem_bytes(n_groups) <= 200 * 1024; }

@@ -6,8 +6,9 @@
 // active counts gives every run its output positions: active tokens go to
 // the prefix in ascending order, inactive tokens after counts[g] in
 // ascending order.  Columns longer than 32 * blockDim tokens are processed in
-// chunks after a counting pass.  This kernel reads each column at a stride of
-// n_groups bytes.
+// chunks after a counting pass.  Each chunk's partition is assembled in shared
+// memory and copied out as two contiguous ranges (coalesced stores).  This
+// kernel reads each column at a stride of n_groups bytes.
 //
 // With a workspace, reorder_coop_kernel does the same partition from
 // coalesced reads of the mask rows instead: a cooperative grid stages each
@@ -60,6 +61,9 @@ __global__ void __launch_bounds__(kThreads)
                    int32_t *__restrict__ perm, int32_t *__restrict__ counts) {
     __shared__ int warp_sums[32];
     __shared__ int s_total;
+    // this chunk's partition (its active tokens, then its inactive ones), copied
+    // out as two contiguous ranges so that the stores coalesce
+    extern __shared__ int32_t s_part[];
     const int g = blockIdx.x;
     const int tid = threadIdx.x;
     const long long chunk = static_cast<long long>(kThreads) * kRun;
@@ -96,13 +100,18 @@ __global__ void __launch_bounds__(kThreads)
         const int chunk_active = s_total;
         if (total < 0) total = chunk_active;  // single chunk: column total known now
         const int tok_before = min(first, len);
-        int pa = run_active + a_off;
-        int pi = total + static_cast<int>(base - run_active) + (tok_before - a_off);
+        int la = a_off;                                  // chunk-local slots
+        int li = chunk_active + (tok_before - a_off);
         for (int j = 0; j < n_tok; ++j) {
             const int t = static_cast<int>(base) + first + j;
-            if ((bits >> j) & 1u) out[pa++] = t;
-            else out[pi++] = t;
+            if ((bits >> j) & 1u) s_part[la++] = t;
+            else s_part[li++] = t;
         }
+        __syncthreads();
+        // active tokens go to run_active.., inactive ones to total + (inactive before)..
+        const long long ina_dst = total + (base - run_active) - chunk_active;
+        for (int i = tid; i < len; i += kThreads)
+            out[i < chunk_active ? run_active + i : static_cast<int>(ina_dst + i)] = s_part[i];
         run_active += chunk_active;
         __syncthreads();
     }
@@ -180,7 +189,12 @@ cudaError_t launch_reorder_coop(const uint8_t *mask, int T, int n_groups, int32_
 
 cudaError_t launch_reorder(const uint8_t *mask, int T, int n_groups, int32_t *perm,
                            int32_t *counts, cudaStream_t s) {
-    reorder_kernel<<<n_groups, kThreads, 0, s>>>(mask, T, n_groups, perm, counts);
+    const long long chunk = static_cast<long long>(kThreads) * kRun;
+    const int smem = static_cast<int>((T < chunk ? T : chunk) * sizeof(int32_t));
+    cudaError_t e = cudaFuncSetAttribute(reorder_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(chunk * sizeof(int32_t)));
+    if (e != cudaSuccess) return e;
+    reorder_kernel<<<n_groups, kThreads, smem, s>>>(mask, T, n_groups, perm, counts);
     return cudaGetLastError();
 }
 

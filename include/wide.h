@@ -82,8 +82,8 @@ int wide_num_sms(void);
  *            otherwise (ws NULL or smaller, or a grid that cannot be
  *            resident) one block per column walks its column.  Same result
  *            either way.  wide_reorder_workspace_size() returns that size
- *            where the cooperative launch measured faster (T >= 49152, or
- *            T >= 16384 with n_groups <= 32), else 0.
+ *            where the cooperative launch measured faster (T >= 65536, or
+ *            T >= 16384 with n_groups <= 16), else 0.
  * Bit-exact and deterministic.  T <= 2^31 - 1, 1 <= n_groups <= 65535.
  */
 wide_status_t wide_reorder_masks(const uint8_t *mask, int T, int n_groups,
