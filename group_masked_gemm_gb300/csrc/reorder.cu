@@ -87,7 +87,7 @@ __global__ void __launch_bounds__(kThreads)
         const int first = tid * R;                      // offset inside the chunk
         const int n_tok = max(0, min(R, len - first));
         uint32_t bits = 0;
-#pragma unroll 8
+#pragma unroll
         for (int j = 0; j < kRun; ++j) {
             if (j < n_tok) {
                 const size_t t = static_cast<size_t>(base + first + j);
