@@ -6,7 +6,8 @@
 // GB300 design: a persistent CTA owns an output tile of 128 tokens (natural
 // order) x BN columns and keeps its fp32 accumulator in TMEM for the whole
 // reduction, adding the groups in ascending order -- a per-token ordered
-// reduction with no atomics, no workspace and a deterministic result.  The
+// reduction with no atomics and a deterministic result (a workspace only for
+// the split cases below).  The
 // routing mask is applied inside the tensor core: every tcgen05.mma of group
 // g carries a disable-output-lane mask whose bit is set for the tokens of the
 // tile with M[t,g] = 0, so their accumulator rows are left untouched (the
@@ -28,6 +29,13 @@
 // items per output tile (so a sparse mask does not leave a few CTAs with most
 // of the live weights); each item writes fp32 partial sums, added in split
 // order by a finalize kernel.
+//
+// Prefill takes tiles round-robin, so its last wave holds items mod
+// num_SMs tiles.  When that wave would leave at least half of the SMs idle
+// and the caller passed the optional workspace, each of its tiles is cut
+// into equal shares of its live groups (the tail split): the shares write
+// fp32 partials to a compact array, and gemm_k_tail_finalize_kernel adds
+// them in share order.
 #include "common.cuh"
 #include "internal.h"
 
